@@ -1,0 +1,148 @@
+/*
+ * ssd_scan.h -- C ABI of the GB300 (sm_103a) Mamba2 SSD varlen scan library.
+ *
+ * The operation (one call = one Mamba2 layer's SSD scan over a packed batch):
+ * the chunked SSD scan of Mamba2 prefill, continued prefill and MTP
+ * verification.  The pages run it as five Triton launches (cumsum, chunk
+ * state, state passing, bmm, chunk scan) or as FlashInfer's fused two-launch
+ * scan over packed cu_seqlens (vLLM PR #61501 "Details"); initial states are
+ * read straight from the cache slot instead of a dense gather (vLLM PR #62922
+ * "Details"); final states are written back in the cache dtype (vLLM PR
+ * #61501 "Details"); MTP keeps the state after every speculative token (vLLM
+ * PR #52928 "Summary").  The pages do not print the recurrence; this library
+ * computes, for sequence s = tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 and
+ * head h (group g = h / (nheads / ngroups)):
+ *
+ *   dt'_t    = softplus(dt[t,h] + dt_bias[h])      if dt_softplus
+ *            = dt[t,h] + dt_bias[h]                 otherwise (bias 0 if NULL)
+ *   h_{-1}   = has_init[s] ? state_cache[slot_idx[s], h] : 0   (fp32 math)
+ *   h_t[p,n] = exp(dt'_t A[h]) h_{t-1}[p,n] + dt'_t x[t,h,p] B[t,g,n]
+ *   y[t,h,p] = sum_n C[t,g,n] h_t[p,n] + D[h] x[t,h,p]          (D 0 if NULL)
+ *   state_cache[slot_idx[s], h] = h_last   (write_final; rounded to nearest
+ *                                           even in the cache dtype)
+ *   out_intermediate[t, h] = h_t           (if not NULL)
+ *
+ * Layouts (all dense, row-major, innermost index last):
+ *   x, out_y         [T, H, P]            io_dtype (F32 or BF16)
+ *   B, C             [T, G, N]            io_dtype
+ *   dt               [T, H]               float32 (raw, before bias/softplus)
+ *   dt_bias, A, D    [H]                  float32 (dt_bias, D may be NULL)
+ *   cu_seqlens       [S+1]                int32, device; cu[0] = 0, cu[S] = T,
+ *                                         non-decreasing (empty sequences ok)
+ *   state_cache      [num_slots, H, P, N] state_dtype (F32, BF16 or F16)
+ *   slot_idx         [S]                  int32, device
+ *   has_init         [S]                  uint8, device, or NULL (= all zero)
+ *   out_intermediate [T, H, P, N]         state_dtype, or NULL
+ * All pointers except `workspace` may be any device-accessible pointer the
+ * kernels can read; the library itself never dereferences them on the host.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates nothing,
+ * frees nothing and never synchronises: a call validates its arguments on
+ * the host, enqueues at most two kernels on `stream` and returns.  Nothing is
+ * read back to the host, so a call may be captured in a CUDA graph.
+ *
+ * Aliasing: state_cache is read (initial states) and written (final states)
+ * in place; a sequence's final state goes into the slot its initial state
+ * came from.  out_y and out_intermediate must not overlap any input.  Two
+ * sequences that name the same slot with write_final = 1 give an undefined
+ * result for that slot.  Slots not named by slot_idx are never read or
+ * written.
+ *
+ * Errors: invalid arguments return an error status and launch nothing.
+ * Metadata that can only be checked on the device (slot index outside
+ * [0, num_slots), cu_seqlens out of range or decreasing) makes the kernels
+ * skip that sequence and OR a flag into *device_status (if not NULL); the
+ * kernels never trap.
+ */
+#ifndef SSD_SCAN_H_
+#define SSD_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* = cudaStream_t */
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* bad size, NULL required pointer, bad dtype */
+    SSD_ERR_UNSUPPORTED = 2,  /* valid but not compiled (e.g. dstate > 256) */
+    SSD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required   */
+    SSD_ERR_CUDA = 4          /* a CUDA runtime/driver call failed          */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype;
+
+/* bits OR-ed into *device_status by the kernels */
+#define SSD_DEV_BAD_SLOT 1        /* slot_idx[s] outside [0, num_slots)        */
+#define SSD_DEV_BAD_SEQLENS 2     /* cu_seqlens[s..s+1] not within [0, T]      */
+#define SSD_DEV_TIMEOUT 4         /* an internal wait of the chunked kernel ran
+                                     out of time; its outputs are incomplete   */
+
+typedef struct {
+    int64_t total_tokens;       /* T                                          */
+    int32_t num_seqs;           /* S                                          */
+    int32_t max_seqlen;         /* host hint, >= every sequence length, or 0
+                                   when unknown; only selects the kernel      */
+    int32_t nheads;             /* H                                          */
+    int32_t headdim;            /* P                                          */
+    int32_t dstate;             /* N                                          */
+    int32_t ngroups;            /* G, divides H                               */
+    int32_t chunk_size;         /* >= 1; the chunked kernel's result does not
+                                   depend on it beyond rounding               */
+    int32_t io_dtype;           /* ssd_dtype of x, B, C, out_y                */
+    int32_t state_dtype;        /* ssd_dtype of state_cache, out_intermediate */
+    int32_t dt_softplus;        /* 1: dt' = softplus(dt + dt_bias)            */
+    int32_t write_final;        /* 1: write h_last into state_cache[slot]    */
+    int32_t num_slots;          /* rows of state_cache                        */
+    int32_t reserved0;
+    const void *x;
+    const float *dt;
+    const float *dt_bias;       /* may be NULL                                */
+    const float *A;
+    const void *B;
+    const void *C;
+    const float *D;             /* may be NULL                                */
+    const int32_t *cu_seqlens;
+    void *state_cache;          /* may be NULL only if no sequence reads or
+                                   writes a slot (has_init NULL, no final)    */
+    const int32_t *slot_idx;    /* may be NULL under the same condition       */
+    const uint8_t *has_init;    /* may be NULL                                */
+    void *out_y;
+    void *out_intermediate;     /* may be NULL                                */
+    void *workspace;            /* device scratch, see workspace_size         */
+    size_t workspace_bytes;
+    int32_t *device_status;     /* device int32 or NULL                       */
+} ssd_scan_params;
+
+/* Bytes of device workspace a call with these parameters needs (a function
+ * of S and the selected kernel only; may be 0).  The workspace must be
+ * 256-byte aligned and is overwritten by the call.  Returns 0 for invalid
+ * parameters as well; ssd_scan_varlen reports those. */
+size_t ssd_scan_varlen_workspace_size(const ssd_scan_params *params);
+
+/* Enqueue the scan on `stream` (NULL = legacy default stream).  Returns
+ * SSD_OK when the kernels were enqueued; launch errors come back as
+ * SSD_ERR_CUDA.  Never synchronises. */
+ssd_status ssd_scan_varlen(const ssd_scan_params *params, struct CUstream_st *stream);
+
+/* Number of kernels a call with these parameters launches (0 for an empty
+ * batch, at most 2), or -1 if the parameters are invalid. */
+int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params);
+
+/* Name of the kernel path a call would take: "chunked_tc" (tcgen05 chunked
+ * scan), "recurrent" (token-by-token SIMT scan: fp32 I/O, intermediate
+ * states, continuations of at most 3 tokens, other shapes) or "invalid". */
+const char *ssd_scan_varlen_path(const ssd_scan_params *params);
+
+/* Static description of a status code. */
+const char *ssd_status_string(ssd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_SCAN_H_ */

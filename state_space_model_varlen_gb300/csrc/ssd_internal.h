@@ -1,0 +1,37 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd_scan.h"
+
+namespace ssd {
+
+// Launch-ready copy of the public parameters (validated on the host).
+struct ScanArgs {
+    int64_t T;
+    int32_t S, H, P, N, G;
+    int32_t heads_per_group;
+    int32_t num_slots;
+    int32_t dt_softplus, write_final;
+    const void *x;
+    const float *dt, *dt_bias, *A, *D;
+    const void *B, *C;
+    const int32_t *cu_seqlens, *slot_idx;
+    const uint8_t *has_init;
+    void *state_cache, *out_y, *out_intermediate;
+    int32_t *device_status;
+};
+
+// Token-by-token SIMT scan (any shape with N <= 256, any dtype).  One launch.
+cudaError_t launch_recurrent(const ScanArgs &a, int io_dtype, int state_dtype,
+                             cudaStream_t stream);
+
+// Chunked tcgen05 scan (bf16 I/O, P = 64, N = 128).  Two launches.
+bool chunked_supported(const ssd_scan_params &p);
+size_t chunked_workspace_bytes(const ssd_scan_params &p);
+cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace,
+                           cudaStream_t stream);
+
+}  // namespace ssd

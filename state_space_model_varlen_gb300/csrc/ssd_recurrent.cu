@@ -1,0 +1,203 @@
+// Token-by-token SIMT scan of the Mamba2 SSD recurrence.
+//
+// This is the "short path" for continuations of a few tokens (MTP
+// verification: one target plus draft tokens per request, vLLM PR #52928
+// "Summary"), where the work is streaming the recurrent state once through
+// the SM, and the general path for shapes and dtypes the chunked tensor-core
+// kernel does not cover (fp32 activations, intermediate states, other
+// head/state sizes).
+//
+// Work split: one CTA per (sequence, head, block of 16 p-rows); warp w owns
+// p-rows [4w, 4w+4) of the block and each lane owns NPL consecutive state
+// columns n, so the whole state slice lives in registers (4 x NPL floats per
+// thread) and one token costs one warp-level reduction per p-row for y.
+// Warps never synchronise with each other.  The initial state is read
+// straight from the cache slot (no gather, vLLM PR #62922 "Details") and the
+// final state is written back into the same slot in the cache dtype with
+// round-to-nearest-even (vLLM PR #61501 "Details").
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+
+// softplus(z) = log(1 + e^z) in the overflow-safe form max(z,0) + log1p(e^-|z|)
+__device__ __forceinline__ float softplus_f(float z) {
+    return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
+}
+
+template <typename IoT, typename StT, int NPL>
+__global__ void __launch_bounds__(kWarps * 32)
+recurrent_scan_kernel(ScanArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int pblocks = (a.P + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t bid = blockIdx.x;
+    const int pb = (int)(bid % pblocks);
+    const int h = (int)((bid / pblocks) % a.H);
+    const int s = (int)(bid / ((int64_t)pblocks * a.H));
+    const int p0 = pb * kRowsPerCta + warp * kRowsPerWarp;
+    if (p0 >= a.P) return;                                   // warp-uniform
+    const int g = h / a.heads_per_group;
+
+    // ---- sequence metadata, checked on the device --------------------------
+    const int64_t t0 = a.cu_seqlens[s];
+    const int64_t t1 = a.cu_seqlens[s + 1];
+    if (t0 < 0 || t1 < t0 || t1 > a.T) {
+        if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
+            atomicOr(a.device_status, SSD_DEV_BAD_SEQLENS);
+        return;
+    }
+    const bool init = a.has_init != nullptr && a.has_init[s] != 0;
+    const bool need_slot = init || a.write_final;
+    int slot = 0;
+    if (need_slot) {
+        slot = a.slot_idx[s];
+        if (slot < 0 || slot >= a.num_slots) {
+            if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
+                atomicOr(a.device_status, SSD_DEV_BAD_SLOT);
+            return;
+        }
+    }
+
+    const int n0 = lane * NPL;
+    bool row_ok[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) row_ok[i] = (p0 + i) < a.P;
+
+    // ---- initial state (fp32 in registers) ---------------------------------
+    float st[kRowsPerWarp][NPL];
+    const StT *cache = static_cast<const StT *>(a.state_cache);
+    const int64_t slot_base = (((int64_t)slot * a.H + h) * a.P) * a.N;
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+            const int n = n0 + j;
+            st[i][j] = (init && row_ok[i] && n < a.N)
+                           ? to_f(cache[slot_base + (int64_t)(p0 + i) * a.N + n]) : 0.f;
+        }
+
+    const IoT *X = static_cast<const IoT *>(a.x);
+    const IoT *Bm = static_cast<const IoT *>(a.B);
+    const IoT *Cm = static_cast<const IoT *>(a.C);
+    IoT *Y = static_cast<IoT *>(a.out_y);
+    StT *inter = static_cast<StT *>(a.out_intermediate);
+    const float Ah = a.A[h];
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+    const float Dh = a.D ? a.D[h] : 0.f;
+
+    for (int64_t t = t0; t < t1; ++t) {
+        const float z = a.dt[t * a.H + h] + bias;
+        const float d = a.dt_softplus ? softplus_f(z) : z;
+        const float decay = expf(d * Ah);
+        float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+        const int64_t xrow = (t * a.H + h) * a.P + p0;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = row_ok[i] ? to_f(X[xrow + i]) : 0.f;
+        const int64_t brow = (t * a.G + g) * a.N;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+            const bool ok = (n0 + j) < a.N;
+            bv[j] = ok ? to_f(Bm[brow + n0 + j]) : 0.f;
+            cv[j] = ok ? to_f(Cm[brow + n0 + j]) : 0.f;
+        }
+        float part[kRowsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const float dx = d * xv[i];
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+                st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+                acc = fmaf(cv[j], st[i][j], acc);
+            }
+            part[i] = acc;
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
+        if (lane < kRowsPerWarp && row_ok[lane]) {
+            float yv = 0.f;
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i)
+                if (i == lane) yv = part[i] + Dh * xv[i];
+            Y[xrow + lane] = from_f<IoT>(yv);
+        }
+        if (inter) {
+            const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i)
+                if (row_ok[i])
+#pragma unroll
+                    for (int j = 0; j < NPL; ++j)
+                        if (n0 + j < a.N)
+                            inter[ibase + (int64_t)i * a.N + n0 + j] = from_f<StT>(st[i][j]);
+        }
+    }
+
+    if (a.write_final) {
+        StT *out = static_cast<StT *>(a.state_cache);
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i)
+            if (row_ok[i])
+#pragma unroll
+                for (int j = 0; j < NPL; ++j)
+                    if (n0 + j < a.N)
+                        out[slot_base + (int64_t)(p0 + i) * a.N + n0 + j] = from_f<StT>(st[i][j]);
+    }
+}
+
+template <typename IoT, typename StT>
+cudaError_t launch_npl(const ScanArgs &a, cudaStream_t stream) {
+    const int pblocks = (a.P + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t blocks = (int64_t)a.S * a.H * pblocks;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks), block(kWarps * 32);
+    if (a.N <= 32) recurrent_scan_kernel<IoT, StT, 1><<<grid, block, 0, stream>>>(a);
+    else if (a.N <= 64) recurrent_scan_kernel<IoT, StT, 2><<<grid, block, 0, stream>>>(a);
+    else if (a.N <= 128) recurrent_scan_kernel<IoT, StT, 4><<<grid, block, 0, stream>>>(a);
+    else recurrent_scan_kernel<IoT, StT, 8><<<grid, block, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename IoT>
+cudaError_t launch_state(const ScanArgs &a, int state_dtype, cudaStream_t stream) {
+    switch (state_dtype) {
+        case SSD_F32: return launch_npl<IoT, float>(a, stream);
+        case SSD_BF16: return launch_npl<IoT, __nv_bfloat16>(a, stream);
+        case SSD_F16: return launch_npl<IoT, __half>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const ScanArgs &a, int io_dtype, int state_dtype,
+                             cudaStream_t stream) {
+    if (io_dtype == SSD_F32) return launch_state<float>(a, state_dtype, stream);
+    if (io_dtype == SSD_BF16) return launch_state<__nv_bfloat16>(a, state_dtype, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ssd

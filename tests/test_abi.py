@@ -1,0 +1,104 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, exports
+every entry point declared in include/ssd_scan.h, the ctypes mirror of
+``ssd_scan_params`` has the C layout, and host-side validation rejects bad
+arguments before anything is enqueued (those calls touch no CUDA API)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from state_space_model_varlen_gb300 import binding, _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd_scan.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    assert sorted(binding.EXPORTED) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIBPATH], capture_output=True,
+                         text=True, check=True).stdout
+    for name in declared:
+        assert re.search(r"\bT %s$" % name, out, re.M), name
+
+
+def test_params_struct_layout_matches_c(tmp_path):
+    fields = [f[0] for f in binding.ScanParams._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "%s"' % HEADER,
+            "int main(void){", 'printf("%zu\\n", sizeof(ssd_scan_params));']
+    for f in fields:
+        prog.append('printf("%%zu\\n", offsetof(ssd_scan_params, %s));' % f)
+    prog.append("return 0;}")
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(prog))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", str(c), "-o", str(exe)], check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(binding.ScanParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(binding.ScanParams, f).offset == off, f
+
+
+def _params(**kw):
+    p = binding.ScanParams()
+    p.total_tokens, p.num_seqs, p.max_seqlen = 10, 2, 0
+    p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = 4, 64, 128, 2, 128
+    p.io_dtype, p.state_dtype = binding.SSD_BF16, binding.SSD_F32
+    p.dt_softplus, p.write_final, p.num_slots = 1, 1, 4
+    for name in ("x", "dt", "A", "B", "C", "cu_seqlens", "state_cache", "slot_idx", "out_y"):
+        setattr(p, name, 0x1000)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value", [
+    ("nheads", 0), ("headdim", -1), ("ngroups", 3), ("chunk_size", 0), ("io_dtype", 2),
+    ("io_dtype", 7), ("state_dtype", 5), ("total_tokens", -1), ("x", None),
+    ("cu_seqlens", None), ("state_cache", None), ("slot_idx", None), ("num_slots", 0),
+])
+def test_invalid_arguments_rejected_without_launch(field, value):
+    p = _params(**{field: value})
+    lib = binding.load()
+    rc = lib.ssd_scan_varlen(ctypes.byref(p), None)
+    assert rc == binding.SSD_ERR_INVALID_ARG
+    assert binding.num_launches(p) == -1
+    assert binding.kernel_path(p) == "invalid"
+    assert binding.workspace_size(p) == 0
+
+
+def test_unsupported_state_size():
+    p = _params(dstate=512)
+    assert binding.load().ssd_scan_varlen(ctypes.byref(p), None) == binding.SSD_ERR_UNSUPPORTED
+
+
+def test_empty_batch_launches_nothing():
+    p = _params(num_seqs=0, total_tokens=0)
+    assert binding.num_launches(p) == 0
+    assert binding.load().ssd_scan_varlen(ctypes.byref(p), None) == binding.SSD_OK
+
+
+def test_kernel_path_selection():
+    assert binding.kernel_path(_params(io_dtype=binding.SSD_F32)) == "recurrent"
+    assert binding.kernel_path(_params(out_intermediate=0x2000)) == "recurrent"
+    assert binding.kernel_path(_params(max_seqlen=3)) == "recurrent"
+    assert binding.num_launches(_params(io_dtype=binding.SSD_F32)) == 1
+
+
+def test_status_strings():
+    for code in range(5):
+        assert binding.status_string(code) and binding.status_string(code) != "unknown status"
+    assert binding.status_string(99) == "unknown status"

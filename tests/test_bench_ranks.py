@@ -1,0 +1,42 @@
+"""The benchmark's multi-rank path (weak scaling, no collective on the data
+path) on CPU with two gloo ranks: timings are reduced with a max and the
+whole-job value counts the tokens of every rank."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = [10.0 + rank * 5.0, 3.0 - rank]
+        got = bench.max_over_ranks(local)
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    world = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    assert out[0] == [15.0, 3.0] and out[1] == [15.0, 3.0]
+
+
+def test_whole_job_rate_counts_all_ranks():
+    assert bench.whole_job_rate(1000, 4, 2.0) == pytest.approx(2e6)
+    assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]     # single process: identity

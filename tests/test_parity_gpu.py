@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Small cases are compared element by element in full;
+the named full-size workloads run in the benchmark's launch configuration and
+are compared on sampled sequences/heads the oracle computes one by one."""
+import numpy as np
+import pytest
+
+import oracle
+from state_space_model_varlen_gb300 import workloads as W
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_and_check(p, **kw):
+    out = Hn.run_gpu(p, **kw)
+    ref = oracle.ssd_scan_reference(p)
+    assert out["status"] == 0
+    Hn.check_all(p, out, ref)
+    return out, ref
+
+
+SMALL = {
+    "tiny_fp32": lambda: W.workload("tiny"),
+    "bf16_ragged": lambda: W.make_problem([1, 5, 127, 128, 129, 300, 0, 513], nheads=8, headdim=64,
+                                          dstate=128, ngroups=2, num_slots=64, seed=31),
+    "bf16_cache_continue": lambda: W.make_problem([32, 200, 1, 0], nheads=8, headdim=64, dstate=128,
+                                                  ngroups=4, state_dtype="bf16", num_slots=16,
+                                                  has_init=[1, 1, 0, 1], cache_std=0.1, seed=32),
+    "fp16_cache_continue": lambda: W.make_problem([70, 3], nheads=4, headdim=64, dstate=128,
+                                                  ngroups=1, state_dtype="f16", num_slots=5,
+                                                  has_init=True, cache_std=0.1, seed=33),
+    "mtp_small": lambda: W.make_problem([3] * 16, nheads=8, headdim=64, dstate=128, ngroups=2,
+                                        num_slots=32, has_init=True, write_final=False,
+                                        want_intermediate=True, cache_std=0.1, seed=34),
+    "no_softplus_no_bias_no_D": lambda: W.make_problem([40, 257], nheads=4, headdim=64, dstate=128,
+                                                       ngroups=2, dt_softplus=False,
+                                                       with_dt_bias=False, with_D=False,
+                                                       num_slots=4, seed=35),
+    "odd_shape_fp32": lambda: W.make_problem([17, 1, 90], nheads=6, headdim=24, dstate=40,
+                                             ngroups=3, io_dtype="f32", num_slots=3,
+                                             has_init=[0, 1, 1], seed=36),
+    "odd_shape_bf16_inter": lambda: W.make_problem([9, 4], nheads=2, headdim=72, dstate=200,
+                                                   ngroups=1, state_dtype="bf16", num_slots=2,
+                                                   want_intermediate=True, seed=37),
+    "no_final_writeback": lambda: W.make_problem([64, 130], nheads=4, headdim=64, dstate=128,
+                                                 ngroups=2, write_final=False, num_slots=2,
+                                                 has_init=True, seed=38),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_parity_small(name):
+    _run_and_check(SMALL[name]())
+
+
+def test_d_zero_checks_scan_part_tightly():
+    """With D = 0, y is the scan part alone, so the 2e-2 rms bound applies to it."""
+    p = W.make_problem([100, 250, 7], nheads=8, headdim=64, dstate=128, ngroups=2, with_D=False,
+                       num_slots=8, has_init=[1, 0, 1], cache_std=0.5, seed=39)
+    _run_and_check(p)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_chunk_size_invariance(chunk):
+    p = W.make_problem([300, 45], nheads=4, headdim=64, dstate=128, ngroups=1, chunk_size=chunk,
+                       num_slots=4, seed=40)
+    _run_and_check(p)
+
+
+def test_sequence_permutation_bit_identical():
+    p = W.make_problem([50, 180, 7, 129], nheads=4, headdim=64, dstate=128, ngroups=2,
+                       num_slots=8, has_init=[1, 0, 1, 0], seed=41)
+    out = Hn.run_gpu(p)
+    order = [2, 0, 3, 1]
+    q = W.select_sequences(p, order)
+    outq = Hn.run_gpu(q)
+    cu, cq = p.cu_seqlens, q.cu_seqlens
+    for j, s in enumerate(order):
+        np.testing.assert_array_equal(outq["y"][cq[j]:cq[j + 1]], out["y"][cu[s]:cu[s + 1]])
+        np.testing.assert_array_equal(outq["cache"][p.slot_idx[s]], out["cache"][p.slot_idx[s]])
+
+
+def test_short_path_hint_agrees_with_general_path():
+    p = W.make_problem([3, 2, 1, 3], nheads=8, headdim=64, dstate=128, ngroups=2, num_slots=8,
+                       has_init=True, cache_std=0.1, seed=42)
+    a = Hn.run_gpu(p, max_seqlen=3)
+    b = Hn.run_gpu(p, max_seqlen=0)
+    ref = oracle.ssd_scan_reference(p)
+    Hn.check_all(p, a, ref)
+    Hn.check_all(p, b, ref)
+
+
+def test_bad_slot_sets_device_status_and_skips_only_that_sequence():
+    p = W.make_problem([20, 30, 10], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
+                       slots=[1, 9, 2], seed=43)
+    out = Hn.run_gpu(p)
+    assert out["status"] & 1
+    good = W.select_sequences(p, [0, 2])
+    ref = oracle.ssd_scan_reference(good)
+    cu = p.cu_seqlens
+    rows = np.r_[cu[0]:cu[1], cu[2]:cu[3]]
+    Hn.check_y(out["y"][rows], ref["y"], p.io_dtype)
+    assert np.all(np.isnan(out["y"][cu[1]:cu[2]]))        # skipped: left unwritten
+    for s, q in ((0, 0), (2, 1)):
+        Hn.check_state(out["cache"][p.slot_idx[s]], ref["final"][q], p.state_dtype)
+    np.testing.assert_array_equal(out["cache"][[0, 3]], p.cache[[0, 3]])
+
+
+def test_bad_cu_seqlens_sets_device_status():
+    p = W.make_problem([20, 30], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=2, seed=44)
+    p.cu_seqlens = np.array([0, 60, 50], dtype=np.int32)    # decreasing, beyond T
+    out = Hn.run_gpu(p, max_seqlen=64)
+    assert out["status"] & 2
+
+
+# ---------------------------------------------------------------------------
+# named full-size workloads: full GPU run, sampled oracle comparison
+# ---------------------------------------------------------------------------
+def _sampled(p, seqs, heads):
+    out = Hn.run_gpu(p)
+    assert out["status"] == 0
+    q = W.select_sequences(p, seqs)
+    ref = oracle.ssd_scan_reference(q, heads=heads)
+    rows = np.concatenate([np.arange(p.cu_seqlens[s], p.cu_seqlens[s + 1]) for s in seqs])
+    h0, h1 = heads
+    Hn.check_y(out["y"][rows][:, h0:h1], ref["y"][:, h0:h1], p.io_dtype)
+    named = set(int(s) for s in p.slot_idx) if p.write_final else set()
+    untouched = [i for i in range(p.num_slots) if i not in named]
+    np.testing.assert_array_equal(out["cache"][untouched], p.cache[untouched])
+    if p.write_final:
+        for j, s in enumerate(seqs):
+            Hn.check_state(out["cache"][p.slot_idx[s], h0:h1], ref["final"][j, h0:h1],
+                           p.state_dtype)
+    if p.want_intermediate:
+        for j, t in enumerate(rows):
+            Hn.check_state(out["inter"][t, h0:h1], ref["inter"][j, h0:h1], p.state_dtype)
+    assert out["launches"] <= 2
+    return out
+
+
+def test_workload_dense_prefill_sampled():
+    _sampled(W.workload("dense_prefill"), [0, 7], (0, 16))
+
+
+def test_workload_varlen_prefill_sampled():
+    p = W.workload("varlen_prefill")
+    lens = p.seqlens
+    order = np.argsort(lens)
+    seqs = sorted(set([int(order[0]), int(order[1]), int(order[-1]), 3, 17]))
+    _sampled(p, seqs, (16, 32))
+
+
+def test_workload_continued_a():
+    _sampled(W.workload("continued_a"), [0], (0, 128))
+
+
+def test_workload_continued_b_sampled():
+    _sampled(W.workload("continued_b"), [0, 1, 2], (0, 32))
+
+
+def test_workload_mtp_sampled():
+    _sampled(W.workload("mtp"), [0, 5, 127], (0, 128))
+
+
+def test_tensor_core_path_is_taken_for_bf16_prefill():
+    """bf16 I/O with headdim 64 / d_state 128 runs the two-launch tcgen05 path."""
+    p = W.make_problem([200, 64], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
+                       seed=45)
+    out, _ = _run_and_check(p)
+    assert out["path"] == "chunked_tc"
+    assert out["launches"] == 2
+    q = W.make_problem([3, 3], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
+                       has_init=True, seed=46)
+    outq = Hn.run_gpu(q, max_seqlen=3)
+    assert outq["path"] == "recurrent" and outq["launches"] == 1
+
+
+def test_many_short_sequences_and_empty_ones():
+    """Varlen batch with more work items than SMs, empty sequences and 1-token tails."""
+    rng = np.random.default_rng(47)
+    lens = rng.integers(0, 300, size=60)
+    lens[::7] = 0
+    lens[1::9] = 1
+    p = W.make_problem(lens, nheads=8, headdim=64, dstate=128, ngroups=2, num_slots=80,
+                       has_init=(rng.random(60) < 0.5).astype(np.uint8), cache_std=0.3, seed=47)
+    _run_and_check(p)
