@@ -38,6 +38,59 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 }
 template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
 
+// NPL consecutive elements <-> floats; one 4/8/16-byte access when `vec`.
+template <typename T, int NPL>
+__device__ __forceinline__ void load_n(const T *src, float (&v)[NPL], int valid, bool vec) {
+    if (vec && valid >= NPL) {
+        constexpr int bytes = NPL * (int)sizeof(T);
+        if constexpr (bytes == 16 || bytes == 8 || bytes == 4 || bytes == 32) {
+            T tmp[NPL];
+            if constexpr (bytes == 32) {
+                *reinterpret_cast<uint4 *>(tmp) = __ldg(reinterpret_cast<const uint4 *>(src));
+                *(reinterpret_cast<uint4 *>(tmp) + 1) = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+            } else if constexpr (bytes == 16) {
+                *reinterpret_cast<uint4 *>(tmp) = __ldg(reinterpret_cast<const uint4 *>(src));
+            } else if constexpr (bytes == 8) {
+                *reinterpret_cast<uint2 *>(tmp) = __ldg(reinterpret_cast<const uint2 *>(src));
+            } else {
+                *reinterpret_cast<uint32_t *>(tmp) = __ldg(reinterpret_cast<const unsigned int *>(src));
+            }
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) v[j] = to_f(tmp[j]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) v[j] = j < valid ? to_f(src[j]) : 0.f;
+}
+
+template <typename T, int NPL>
+__device__ __forceinline__ void store_n(T *dst, const float (&v)[NPL], int valid, bool vec) {
+    T tmp[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) tmp[j] = from_f<T>(v[j]);
+    if (vec && valid >= NPL) {
+        constexpr int bytes = NPL * (int)sizeof(T);
+        if constexpr (bytes == 32) {
+            reinterpret_cast<uint4 *>(dst)[0] = reinterpret_cast<const uint4 *>(tmp)[0];
+            reinterpret_cast<uint4 *>(dst)[1] = reinterpret_cast<const uint4 *>(tmp)[1];
+            return;
+        } else if constexpr (bytes == 16) {
+            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(tmp);
+            return;
+        } else if constexpr (bytes == 8) {
+            *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(tmp);
+            return;
+        } else if constexpr (bytes == 4) {
+            *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(tmp);
+            return;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+        if (j < valid) dst[j] = tmp[j];
+}
+
 // softplus(z) = log(1 + e^z) in the overflow-safe form max(z,0) + log1p(e^-|z|)
 __device__ __forceinline__ float softplus_f(float z) {
     return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
@@ -45,7 +98,7 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 template <typename IoT, typename StT, int NPL>
 __global__ void __launch_bounds__(kWarps * 32)
-recurrent_scan_kernel(ScanArgs a) {
+recurrent_scan_kernel(ScanArgs a, bool vec) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int pblocks = (a.P + kRowsPerCta - 1) / kRowsPerCta;
@@ -86,14 +139,16 @@ recurrent_scan_kernel(ScanArgs a) {
     float st[kRowsPerWarp][NPL];
     const StT *cache = static_cast<const StT *>(a.state_cache);
     const int64_t slot_base = (((int64_t)slot * a.H + h) * a.P) * a.N;
+    const int nvalid = a.N - n0;           // columns of this lane inside [0, N)
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i)
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        if (init && row_ok[i]) {
+            load_n<StT, NPL>(cache + slot_base + (int64_t)(p0 + i) * a.N + n0, st[i], nvalid, vec);
+        } else {
 #pragma unroll
-        for (int j = 0; j < NPL; ++j) {
-            const int n = n0 + j;
-            st[i][j] = (init && row_ok[i] && n < a.N)
-                           ? to_f(cache[slot_base + (int64_t)(p0 + i) * a.N + n]) : 0.f;
+            for (int j = 0; j < NPL; ++j) st[i][j] = 0.f;
         }
+    }
 
     const IoT *X = static_cast<const IoT *>(a.x);
     const IoT *Bm = static_cast<const IoT *>(a.B);
@@ -110,15 +165,10 @@ recurrent_scan_kernel(ScanArgs a) {
         const float decay = expf(d * Ah);
         float xv[kRowsPerWarp], bv[NPL], cv[NPL];
         const int64_t xrow = (t * a.H + h) * a.P + p0;
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = row_ok[i] ? to_f(X[xrow + i]) : 0.f;
+        load_n<IoT, kRowsPerWarp>(X + xrow, xv, a.P - p0, vec);
         const int64_t brow = (t * a.G + g) * a.N;
-#pragma unroll
-        for (int j = 0; j < NPL; ++j) {
-            const bool ok = (n0 + j) < a.N;
-            bv[j] = ok ? to_f(Bm[brow + n0 + j]) : 0.f;
-            cv[j] = ok ? to_f(Cm[brow + n0 + j]) : 0.f;
-        }
+        load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
+        load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
         float part[kRowsPerWarp];
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -147,11 +197,7 @@ recurrent_scan_kernel(ScanArgs a) {
             const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
 #pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i)
-                if (row_ok[i])
-#pragma unroll
-                    for (int j = 0; j < NPL; ++j)
-                        if (n0 + j < a.N)
-                            inter[ibase + (int64_t)i * a.N + n0 + j] = from_f<StT>(st[i][j]);
+                if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
         }
     }
 
@@ -159,12 +205,20 @@ recurrent_scan_kernel(ScanArgs a) {
         StT *out = static_cast<StT *>(a.state_cache);
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i)
-            if (row_ok[i])
-#pragma unroll
-                for (int j = 0; j < NPL; ++j)
-                    if (n0 + j < a.N)
-                        out[slot_base + (int64_t)(p0 + i) * a.N + n0 + j] = from_f<StT>(st[i][j]);
+            if (row_ok[i]) store_n<StT, NPL>(out + slot_base + (int64_t)(p0 + i) * a.N + n0, st[i], nvalid, vec);
     }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename IoT, typename StT, int NPL>
+cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t stream) {
+    // vector accesses need every row start aligned to the vector width
+    const bool vec = (a.N % NPL == 0) && (a.P % kRowsPerWarp == 0) && aligned16(a.x) &&
+                     aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
+                     aligned16(a.out_intermediate);
+    recurrent_scan_kernel<IoT, StT, NPL><<<grid, block, 0, stream>>>(a, vec);
+    return cudaGetLastError();
 }
 
 template <typename IoT, typename StT>
@@ -174,11 +228,10 @@ cudaError_t launch_npl(const ScanArgs &a, cudaStream_t stream) {
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks), block(kWarps * 32);
-    if (a.N <= 32) recurrent_scan_kernel<IoT, StT, 1><<<grid, block, 0, stream>>>(a);
-    else if (a.N <= 64) recurrent_scan_kernel<IoT, StT, 2><<<grid, block, 0, stream>>>(a);
-    else if (a.N <= 128) recurrent_scan_kernel<IoT, StT, 4><<<grid, block, 0, stream>>>(a);
-    else recurrent_scan_kernel<IoT, StT, 8><<<grid, block, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (a.N <= 32) return launch_one<IoT, StT, 1>(a, grid, block, stream);
+    if (a.N <= 64) return launch_one<IoT, StT, 2>(a, grid, block, stream);
+    if (a.N <= 128) return launch_one<IoT, StT, 4>(a, grid, block, stream);
+    return launch_one<IoT, StT, 8>(a, grid, block, stream);
 }
 
 template <typename IoT>
