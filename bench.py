@@ -263,9 +263,9 @@ def run_ours(args, rank, world, local_rank):
         d2h += hinter.numel() * hinter.element_size()
     e2e_steps = max(3, min(args.steps, 20))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    slots64 = slots.long()
+
+    def e2e_step():
         x.copy_(hx, non_blocking=True)
         B.copy_(hB, non_blocking=True)
         C.copy_(hC, non_blocking=True)
@@ -273,9 +273,16 @@ def run_ours(args, rank, world, local_rank):
         ssd.call(params, sptr)
         hy.copy_(y, non_blocking=True)
         if p.write_final:
-            hfinal.copy_(cache.index_select(0, slots), non_blocking=True)
+            hfinal.copy_(cache.index_select(0, slots64), non_blocking=True)
         if inter is not None:
             hinter.copy_(inter, non_blocking=True)
+
+    for _ in range(2):                    # untimed: first-use costs of the copy path
+        e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps

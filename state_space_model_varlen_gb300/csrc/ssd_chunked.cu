@@ -12,27 +12,30 @@
 //   workspace (the only scratch memory), so the persistent CTAs below take
 //   the long chains first.
 // Launch 2 (scan): one persistent CTA per SM.  A work item is one sequence and
-//   two heads of the same B/C group; its tokens are walked in 128-token blocks
-//   and the recurrent state h [2 heads x 64 x 128] never leaves the SM (fp32 in
-//   registers).  Per block, with cum_t = sum_{r<=t} dt'_r A (within the block):
-//     G   = C B^T                         tcgen05, K = n, fp32 in TMEM
-//     S_h = G o exp(cum_t - cum_s) dt'_s  (s <= t), bf16, written back in TMEM
-//     Y   = C h^T                         tcgen05 (state entering the block)
-//     Y  *= exp(cum_t)                    per row and head, in TMEM
-//     Y  += S_h X_h                       tcgen05, A operand from TMEM
-//     y   = Y + D x                       bf16, TMA store
-//     Sc  = Xw^T B,  Xw = exp(cum_end - cum_s) dt'_s x_s split into bf16 hi+lo
-//     h   = exp(cum_end) h + Sc           fp32, written to the cache slot at the end
-//   The hi/lo split keeps the state contributions accurate to ~2^-16 so final
-//   states meet fp32-storage accuracy; everything else runs on bf16 operands
-//   with fp32 accumulation.
+//   two heads of the same B/C group; its tokens are walked in 128-token blocks.
+//   The recurrent state h [2 heads x 64 x 128] never leaves the SM: it lives in
+//   tensor memory as an fp32 MMA accumulator.  Per block, with
+//   cum_t = sum_{r<=t} dt'_r A (within the block) and Xw_s = exp(cum_end - cum_s) dt'_s x_s:
+//     G   = C B^T                          tcgen05, fp32 in TMEM
+//     S_h = G o exp(cum_t - cum_s) dt'_s   (s <= t) bf16, written back in TMEM
+//     Y   = C h^T                          tcgen05, state entering the block (bf16 copy)
+//     Y  *= exp(cum_t)                     per row and head, in TMEM
+//     Y  += S_h X_h                        tcgen05, A operand from TMEM
+//     y   = Y + D x                        bf16
+//     h   = exp(cum_end) h + B^T Xw        tcgen05 accumulating into the state,
+//                                          Xw split into bf16 hi + lo
+//   The hi/lo split keeps the state contributions accurate to ~2^-16, so final
+//   states meet fp32-storage accuracy; the y path runs on bf16 operands with
+//   fp32 accumulation.  Y is double buffered in TMEM so block k+1's C h^T can
+//   start while block k's epilogue drains.
 //
-// Warp roles (16 warps): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
-// owner, warps 4-7 "token" warpgroup (dt softplus + cumsum, S, row scaling,
-// epilogue; lane = token), warps 8-15 "state" warpgroups (Xw^T, state update,
-// cache I/O; lane = head x p, each warpgroup one half of the 128 state columns).
-// All hand-offs are mbarriers; every wait is bounded and sets an abort flag
-// plus SSD_DEV_TIMEOUT in device_status instead of hanging.
+// Warp roles (16 warps): warp 0 TMA producer, warp 1 MMA issuer, warps 2-3 dt
+// softplus + within-block cumsum (running a block ahead), warps 4-7 "Xw/S"
+// (lane = token), warps 8-11 "epilogue" (lane = token: row scaling, y = Y + D x,
+// stores), warps 12-15 "state" (lane = state column n: state in TMEM, bf16
+// copy for C h^T, per-block decay, cache I/O).  All hand-offs are mbarriers;
+// every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT in
+// device_status instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -51,23 +54,24 @@ using namespace sm100;
 constexpr int kQ = 128;            // tokens per block
 constexpr int kP = 64;             // head dim
 constexpr int kN = 128;            // state dim
-constexpr int kSlots = 5;          // TMA ring of 32 KB tiles (B, C, X per block)
+constexpr int kSlots = 5;          // TMA ring of 32 KB tiles (C, B, X per block)
 constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
+constexpr int kHbufHead = 8192;    // one head of the half-n bf16 state copy: 64 rows x 128 B
 constexpr int kThreads = 512;
 constexpr uint64_t kSpinLimit = 4000000000ull;   // clock cycles (~2 s) per wait
+constexpr float kDiagFactorLimit = 80.f;         // |decay| of a 32-token block for the
+                                                 // factored diagonal path (e^80 < fp32 max)
 
 // TMEM columns
 constexpr uint32_t kColG = 0;      // G / S (in place), lanes = tokens
-constexpr uint32_t kColY = 128;    // Y, lanes = tokens, cols = head x p
-constexpr uint32_t kColSc = 256;   // state contributions, lanes = head x p, cols = n
-constexpr uint32_t kColXhi = 384;  // Xw^T hi, lanes = head x p, cols = s/2
-constexpr uint32_t kColXlo = 448;  // Xw^T lo
+constexpr uint32_t kColY = 128;    // Y[2] at 128 + 128 b, lanes = tokens, cols = head x p
+constexpr uint32_t kColH = 384;    // state, lanes = n, cols = head x p
 
 constexpr uint32_t kIdG = idesc_bf16(128, 128, false, false);    // C . B^T
-constexpr uint32_t kIdY = idesc_bf16(128, 128, false, false);    // C . h^T
+constexpr uint32_t kIdY = idesc_bf16(128, 128, false, true);     // C . h^T, h MN-major
 constexpr uint32_t kIdSX = idesc_bf16(128, 64, false, true);     // S_h . X_h
-constexpr uint32_t kIdSc = idesc_bf16(128, 128, false, true);    // Xw^T . B
+constexpr uint32_t kIdH = idesc_bf16(128, 128, true, true);      // B^T . Xw
 
 struct Params {
     int64_t T;
@@ -77,22 +81,32 @@ struct Params {
     const int32_t *cu_seqlens, *slot_idx, *order;
     const uint8_t *has_init;
     void *state_cache, *out_y;
+    const void *x;
     int32_t *device_status;
 };
 
+// per-block decay arrays, written by the dt warps
+struct Arrays {
+    float cum[2][kQ];      // [head][token] within-block cumsum of dt' A
+    float dtp[2][kQ];      // dt'
+    float vfac[2][kQ];     // exp(cum at end of s's 32-block - cum_s) dt'_s
+    float vdiag[2][kQ];    // exp(cum before s's 32-block - cum_s) dt'_s
+    float cumE[2][4];      // cum at the end of each 32-token block
+    float wtot[2][2];      // scan scratch [head][dt warp]
+    int32_t exact[2][4];   // diagonal block needs the per-element path
+};
+
 struct __align__(1024) Smem {
-    uint8_t slot[kSlots][kTileBytes];     // TMA ring
-    uint8_t hbuf[2][kHalfBytes];          // h (bf16) K-major: [n half][row = head*64+p][128 B]
-    float cum[2][2][kQ];                  // [array buffer][head][token]
-    float dtp[2][2][kQ];                  // dt'
-    float vfac[2][2][kQ];                 // exp(cum_{end of 32-block} - cum_s) dt'_s
-    float wfac[2][2][kQ];                 // exp(cum_end - cum_s) dt'_s
-    float cumE[2][2][4];                  // cum at the end of each 32-token block
-    float wtot[2][2][4];                  // scan scratch [buffer][head][warp]
+    uint8_t slot[kSlots][kTileBytes];     // TMA ring: C / B [n half][s][n], X [head][s][p]
+    uint8_t xw[2][kHalfBytes];            // Xw (hi, then lo), [head][s][p], 128-B swizzle
+    uint8_t hbuf[2 * kHbufHead];          // bf16 h, one half of n at a time: [head][n % 64][p]
+    Arrays arr[2];
     uint64_t full[kSlots], empty[kSlots];
-    uint64_t scan_bar[2], dt_ready[2], arrays_free[2];
-    uint64_t g_ready, s_ready, hs_ready, yinter_ready, y_scaled, y_ready, y_free, ytile;
-    uint64_t xp_ready, sc_ready, sc_free, drain;
+    uint64_t arr_ready[2], arr_free[2], dt_scan[2];
+    uint64_t g_ready, s_ready, xhi_ready, xlo_ready, xbuf_free;
+    uint64_t hs_a, hs_b, hbuf_a_done, state_ready, state_done;
+    uint64_t yinter_ready, y_scaled, y_ready, y_free[2], x_epi_done[2];
+    uint64_t drain;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -111,7 +125,6 @@ struct Walker {
     const Params *p;
     int cta, grid;
     int round = 0;
-    // current item
     bool have = false;
     int32_t seq = 0, h0 = 0, g = 0, slot = 0, len = 0, nb = 0, b = 0;
     int64_t t0 = 0;
@@ -119,7 +132,7 @@ struct Walker {
 
     __device__ Walker(const Params *pp) : p(pp), cta(blockIdx.x), grid(gridDim.x) {}
 
-    // Load the next valid item; returns false when this CTA has no more work.
+    // Next valid item (longest sequences first, snake order over the CTAs).
     __device__ bool next_item(bool report) {
         const int hp_per_seq = p->H / 2;
         while (true) {
@@ -243,78 +256,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <typename StT> __device__ __forceinline__ void load_state_row(const StT *src, float (&h)[64]);
-template <> __device__ __forceinline__ void load_state_row<float>(const float *src, float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
-        h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
-    }
+template <typename StT> __device__ __forceinline__ float load_state(const StT *p);
+template <> __device__ __forceinline__ float load_state<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float load_state<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
 }
-template <> __device__ __forceinline__ void load_state_row<__nv_bfloat16>(const __nv_bfloat16 *src, float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) { h[8 * i + 2 * q] = bf16_lo(w[q]); h[8 * i + 2 * q + 1] = bf16_hi(w[q]); }
-    }
+template <> __device__ __forceinline__ float load_state<__half>(const __half *p) {
+    return __half2float(*p);
 }
-template <> __device__ __forceinline__ void load_state_row<__half>(const __half *src, float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __half2 hh = *reinterpret_cast<const __half2 *>(&w[q]);
-            const float2 f = __half22float2(hh);
-            h[8 * i + 2 * q] = f.x; h[8 * i + 2 * q + 1] = f.y;
-        }
-    }
+template <typename StT> __device__ __forceinline__ void store_state(StT *p, float v);
+template <> __device__ __forceinline__ void store_state<float>(float *p, float v) { *p = v; }
+template <> __device__ __forceinline__ void store_state<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
+    *p = __float2bfloat16_rn(v);
 }
-
-template <typename StT> __device__ __forceinline__ void store_state_row(StT *dst, const float (&h)[64]);
-template <> __device__ __forceinline__ void store_state_row<float>(float *dst, const float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        reinterpret_cast<float4 *>(dst)[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-}
-template <> __device__ __forceinline__ void store_state_row<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint4 v;
-        v.x = pack_bf16(h[8 * i], h[8 * i + 1]);
-        v.y = pack_bf16(h[8 * i + 2], h[8 * i + 3]);
-        v.z = pack_bf16(h[8 * i + 4], h[8 * i + 5]);
-        v.w = pack_bf16(h[8 * i + 6], h[8 * i + 7]);
-        reinterpret_cast<uint4 *>(dst)[i] = v;
-    }
-}
-template <> __device__ __forceinline__ void store_state_row<__half>(__half *dst, const float (&h)[64]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __half2 hh = __floats2half2_rn(h[8 * i + 2 * q], h[8 * i + 2 * q + 1]);
-            w[q] = *reinterpret_cast<const uint32_t *>(&hh);
-        }
-        reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
-// bf16 copy of this thread's 64 state columns into its K-major hbuf row.
-__device__ __forceinline__ void write_hbuf_row(uint8_t *row, int r, const float (&h)[64]) {
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        uint4 v;
-        v.x = pack_bf16(h[8 * cc + 0], h[8 * cc + 1]);
-        v.y = pack_bf16(h[8 * cc + 2], h[8 * cc + 3]);
-        v.z = pack_bf16(h[8 * cc + 4], h[8 * cc + 5]);
-        v.w = pack_bf16(h[8 * cc + 6], h[8 * cc + 7]);
-        *reinterpret_cast<uint4 *>(row + ((cc ^ (r & 7)) << 4)) = v;
-    }
+template <> __device__ __forceinline__ void store_state<__half>(__half *p, float v) {
+    *p = __float2half_rn(v);
 }
 
 // ---------------------------------------------------------------------------
@@ -349,34 +305,43 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
 // ---------------------------------------------------------------------------
 // launch 2: the scan
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16(v.x, v.y); }
+
 template <typename StT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-                    const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_y,
-                    const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap map_c, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 2); }
+        for (int i = 0; i < kSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.scan_bar[i], 4);
-            mbar_init(&sm.dt_ready[i], 4);
-            mbar_init(&sm.arrays_free[i], 12);
+            mbar_init(&sm.arr_ready[i], 2);
+            mbar_init(&sm.arr_free[i], 12);
+            mbar_init(&sm.dt_scan[i], 2);
+            mbar_init(&sm.y_free[i], 4);
         }
         mbar_init(&sm.g_ready, 1);
         mbar_init(&sm.s_ready, 4);
-        mbar_init(&sm.hs_ready, 8);
+        mbar_init(&sm.xhi_ready, 4);
+        mbar_init(&sm.xlo_ready, 4);
+        mbar_init(&sm.xbuf_free, 1);
+        mbar_init(&sm.hs_a, 2);
+        mbar_init(&sm.hs_b, 2);
+        mbar_init(&sm.hbuf_a_done, 1);
+        mbar_init(&sm.state_ready, 4);
+        mbar_init(&sm.state_done, 1);
         mbar_init(&sm.yinter_ready, 1);
         mbar_init(&sm.y_scaled, 4);
         mbar_init(&sm.y_ready, 1);
-        mbar_init(&sm.y_free, 4);
-        mbar_init(&sm.ytile, 4);
-        mbar_init(&sm.xp_ready, 8);
-        mbar_init(&sm.sc_ready, 1);
-        mbar_init(&sm.sc_free, 8);
+        mbar_init(&sm.x_epi_done[0], 4);
+        mbar_init(&sm.x_epi_done[1], 4);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -397,28 +362,36 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_b);
             tma_prefetch_desc(&map_c);
-            tma_prefetch_desc(&map_y);
             Walker wk(&p);
             Chunk c;
             uint32_t kc = 0, issued = 0;
             bool ok = true;
             while (ok && wk.next(c, false, true)) {
                 const int32_t row = (int32_t)c.row0;
-                for (int j = 0; j < 3; ++j) {
+                for (int j = 0; j < 3; ++j) {                    // C, B, X
                     const uint32_t tile = 3 * kc + j, slot = tile % kSlots, use = tile / kSlots;
-                    if (use > 0 && !(ok = wait_bar(sm, &sm.empty[slot], (use - 1) & 1, status))) break;
-                    mbar_arrive_expect_tx(&sm.full[slot], kTileBytes);
-                    uint8_t *dst = sm.slot[slot];
-                    const CUtensorMap *m = (j == 0) ? &map_b : (j == 1) ? &map_c : &map_x;
+                    const CUtensorMap *m = (j == 0) ? &map_c : (j == 1) ? &map_b : &map_x;
                     const int32_t c0 = (j == 2) ? c.h0 * kP : c.g * kN;
                     const int32_t c1 = (j == 2) ? (c.h0 + 1) * kP : c.g * kN + 64;
+                    if (use > 0 && !mbar_try_wait(&sm.empty[slot], (use - 1) & 1)) {
+                        // slot still busy: warm L2 with this tile while waiting
+                        tma_prefetch_l2_2d(m, c0, row);
+                        tma_prefetch_l2_2d(m, c1, row);
+                        if (!(ok = wait_bar(sm, &sm.empty[slot], (use - 1) & 1, status))) break;
+                    }
+                    if (use > 0 && (tile - kSlots) % 3 == 2) {
+                        // previous occupant was an X tile: the epilogue also reads it
+                        const uint32_t pk = (tile - kSlots) / 3;
+                        if (!(ok = wait_bar(sm, &sm.x_epi_done[pk & 1], (pk >> 1) & 1, status))) break;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[slot], kTileBytes);
+                    uint8_t *dst = sm.slot[slot];
                     tma_load_2d(dst, m, &sm.full[slot], c0, row);
                     tma_load_2d(dst + kHalfBytes, m, &sm.full[slot], c1, row);
                     issued = tile + 1;
                 }
                 ++kc;
             }
-            // every issued load must have landed before the CTA exits
             for (uint32_t t = (issued > (uint32_t)kSlots ? issued - kSlots : 0); t < issued; ++t)
                 wait_bar(sm, &sm.full[t % kSlots], (t / kSlots) & 1, nullptr);
         }
@@ -429,14 +402,17 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             Chunk c;
             uint32_t kc = 0;
             bool ok = true;
+            const uint32_t bH = smem_u32(sm.hbuf);
+            const uint32_t bW = smem_u32(sm.xw[0]);
             while (ok && wk.next(c, false)) {
-                const uint32_t tb = 3 * kc, tcc = 3 * kc + 1, tx = 3 * kc + 2;
-                const uint32_t bB = smem_u32(sm.slot[tb % kSlots]);
-                const uint32_t bC = smem_u32(sm.slot[tcc % kSlots]);
-                const uint32_t bX = smem_u32(sm.slot[tx % kSlots]);
+                const uint32_t tC = 3 * kc, tB = 3 * kc + 1, tX = 3 * kc + 2;
+                const uint32_t bC = smem_u32(sm.slot[tC % kSlots]);
+                const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
+                const uint32_t bX = smem_u32(sm.slot[tX % kSlots]);
+                const uint32_t ycol = kColY + 128 * (kc & 1);
                 // ---- G = C B^T ----
-                if (!(ok = wait_bar(sm, &sm.full[tb % kSlots], (tb / kSlots) & 1, status) &&
-                           wait_bar(sm, &sm.full[tcc % kSlots], (tcc / kSlots) & 1, status)))
+                if (!(ok = wait_bar(sm, &sm.full[tC % kSlots], (tC / kSlots) & 1, status) &&
+                           wait_bar(sm, &sm.full[tB % kSlots], (tB / kSlots) & 1, status)))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -446,37 +422,37 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            smem_desc_sw128(bB + off, 16, 1024), kIdG, ks > 0);
                 }
                 mma_commit(&sm.g_ready);
-                // ---- Y = C h^T ----
-                if (!(ok = wait_bar(sm, &sm.hs_ready, kc & 1, status) &&
-                           (kc == 0 || wait_bar(sm, &sm.y_free, (kc - 1) & 1, status))))
+                // ---- Y[b] = C h^T, first half of the state columns n ----
+                if (!(ok = wait_bar(sm, &sm.hs_a, kc & 1, status) &&
+                           (kc < 2 || wait_bar(sm, &sm.y_free[kc & 1], ((kc >> 1) - 1) & 1, status))))
                     break;
                 tc_fence_after();
-                const uint32_t bH = smem_u32(sm.hbuf[0]);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    mma_ss(tmem + kColY, smem_desc_sw128(bC + off, 16, 1024),
-                           smem_desc_sw128(bH + off, 16, 1024), kIdY, ks > 0);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ss(tmem + ycol, smem_desc_sw128(bC + ks * 32, 16, 1024),
+                           smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, ks > 0);
+                mma_commit(&sm.hbuf_a_done);
+                // ---- h += B^T Xw_hi ----
+                if (!(ok = wait_bar(sm, &sm.xhi_ready, kc & 1, status) &&
+                           wait_bar(sm, &sm.state_ready, kc & 1, status)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
+                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
+                mma_commit(&sm.xbuf_free);
+                // ---- Y[b] += C h^T, second half of n ----
+                if (!(ok = wait_bar(sm, &sm.hs_b, kc & 1, status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ss(tmem + ycol, smem_desc_sw128(bC + kHalfBytes + ks * 32, 16, 1024),
+                           smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, 1);
                 mma_commit(&sm.yinter_ready);
-                mma_commit(&sm.empty[tcc % kSlots]);
-                mma_commit(&sm.empty[tcc % kSlots]);
-                // ---- Sc = Xw^T B (hi + lo) ----
-                if (!(ok = wait_bar(sm, &sm.xp_ready, kc & 1, status) &&
-                           (kc == 0 || wait_bar(sm, &sm.sc_free, (kc - 1) & 1, status))))
-                    break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const uint32_t acol = (ks < 8 ? kColXhi : kColXlo) + 8 * (ks & 7);
-                    mma_ts(tmem + kColSc, tmem + acol,
-                           smem_desc_sw128(bB + (ks & 7) * 2048, kHalfBytes, 1024), kIdSc, ks > 0);
-                }
-                mma_commit(&sm.sc_ready);
-                mma_commit(&sm.empty[tb % kSlots]);
-                mma_commit(&sm.empty[tb % kSlots]);
-                // ---- Y += S_h X_h ----
-                if (!(ok = wait_bar(sm, &sm.full[tx % kSlots], (tx / kSlots) & 1, status) &&
+                mma_commit(&sm.empty[tC % kSlots]);
+                // ---- Y[b] += S_h X_h ----
+                if (!(ok = wait_bar(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status) &&
                            wait_bar(sm, &sm.s_ready, kc & 1, status) &&
                            wait_bar(sm, &sm.y_scaled, kc & 1, status)))
                     break;
@@ -486,337 +462,425 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t acol = kColG + 32 * (ks >> 1) + 16 * hh + 8 * (ks & 1);
-                        mma_ts(tmem + kColY + 64 * hh, tmem + acol,
+                        mma_ts(tmem + ycol + 64 * hh, tmem + acol,
                                smem_desc_sw128(bX + hh * kHalfBytes + ks * 2048, 1024, 1024), kIdSX, 1);
                     }
                 }
                 mma_commit(&sm.y_ready);
-                mma_commit(&sm.empty[tx % kSlots]);
+                // ---- h += B^T Xw_lo ----
+                if (!(ok = wait_bar(sm, &sm.xlo_ready, kc & 1, status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
+                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
+                mma_commit(&sm.state_done);
+                mma_commit(&sm.xbuf_free);
+                mma_commit(&sm.empty[tB % kSlots]);
+                mma_commit(&sm.empty[tX % kSlots]);     // the Xw passes have read X by now
                 ++kc;
             }
-            // drain the tensor pipe before TMEM is released
             mma_commit(&sm.drain);
             wait_bar(sm, &sm.drain, 0, nullptr);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ===================== token warpgroup =====================
-        const int q = warp - 4;                 // lane quarter
-        const int t = q * 32 + lane;            // token row within the block
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    } else if (warp == 2 || warp == 3) {
+        // ===================== dt softplus + cumsum (a block ahead) =====================
+        const int dw = warp - 2;
+        const int i = dw * 32 + lane;             // tokens 2i, 2i+1
         Walker wk(&p);
-        Chunk cur, nxt;
-        bool have_cur = wk.next(cur, false);
-        bool have_nxt = have_cur && wk.next(nxt, false);
+        Chunk c;
         uint32_t kc = 0;
-        bool ok = true;
-
-        // dt softplus + within-block cumsum of dt' A for block k -> array buffer k % 2
-        auto dtprep = [&](const Chunk &c, uint32_t k) -> bool {
-            const int ab = k & 1;
-            if (k >= 2 && !warp_wait(sm, &sm.arrays_free[ab], ((k >> 1) - 1) & 1, status)) return false;
-            const bool valid = t < c.l;
-            float d[2] = {0.f, 0.f}, a[2] = {0.f, 0.f};
-            if (valid) {
-                const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (c.row0 + t) * p.H + c.h0);
-                const float rv[2] = {raw.x, raw.y};
+        while (wk.next(c, false)) {
+            const int ab = kc & 1;
+            Arrays &ar = sm.arr[ab];
+            if (kc >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((kc >> 1) - 1) & 1, status)) break;
+            float d[2][2] = {{0.f, 0.f}, {0.f, 0.f}};       // [token][head]
+            const float bias0 = p.dt_bias ? p.dt_bias[c.h0] : 0.f;
+            const float bias1 = p.dt_bias ? p.dt_bias[c.h0 + 1] : 0.f;
+            const float A0 = p.A[c.h0], A1 = p.A[c.h0 + 1];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const float z = rv[hh] + (p.dt_bias ? p.dt_bias[c.h0 + hh] : 0.f);
-                    d[hh] = p.dt_softplus ? softplus_f(z) : z;
-                    a[hh] = d[hh] * p.A[c.h0 + hh];
+            for (int e = 0; e < 2; ++e) {
+                const int tok = 2 * i + e;
+                if (tok < c.l) {
+                    const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (c.row0 + tok) * p.H + c.h0);
+                    const float z0 = raw.x + bias0, z1 = raw.y + bias1;
+                    d[e][0] = p.dt_softplus ? softplus_f(z0) : z0;
+                    d[e][1] = p.dt_softplus ? softplus_f(z1) : z1;
                 }
             }
+            float cum[2][2];                              // [token][head]
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+                const float Ah = hh ? A1 : A0;
+                const float a0 = d[0][hh] * Ah, a1 = d[1][hh] * Ah;
+                float s = a0 + a1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const float v = __shfl_up_sync(0xffffffffu, a[hh], off);
-                    if (lane >= off) a[hh] += v;
+                    const float v = __shfl_up_sync(0xffffffffu, s, off);
+                    if (lane >= off) s += v;
                 }
-                if (lane == 31) sm.wtot[ab][hh][q] = a[hh];
+                cum[1][hh] = s;
+                cum[0][hh] = s - a1;
+                if (lane == 31) ar.wtot[hh][dw] = s;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.scan_bar[ab]);
-            if (!warp_wait(sm, &sm.scan_bar[ab], (k >> 1) & 1, status)) return false;
+            if (lane == 0) mbar_arrive(&sm.dt_scan[ab]);
+            if (!warp_wait(sm, &sm.dt_scan[ab], (kc >> 1) & 1, status)) break;
+            float pre[2], bend[2][2];                     // cum at the end of this warp's two 32-blocks
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float w0 = sm.wtot[ab][hh][0], w1 = sm.wtot[ab][hh][1];
-                const float w2 = sm.wtot[ab][hh][2], w3 = sm.wtot[ab][hh][3];
-                const float e0 = w0, e1 = w0 + w1, e2 = e1 + w2, e3 = e2 + w3;
-                const float pre = (q == 0) ? 0.f : (q == 1) ? e0 : (q == 2) ? e1 : e2;
-                const float cblk = (q == 0) ? e0 : (q == 1) ? e1 : (q == 2) ? e2 : e3;
-                const float cum = a[hh] + pre;
-                sm.cum[ab][hh][t] = cum;
-                sm.dtp[ab][hh][t] = d[hh];
-                sm.vfac[ab][hh][t] = valid ? __expf(cblk - cum) * d[hh] : 0.f;
-                sm.wfac[ab][hh][t] = valid ? __expf(e3 - cum) * d[hh] : 0.f;
-                if (t == 0) {
-                    sm.cumE[ab][hh][0] = e0; sm.cumE[ab][hh][1] = e1;
-                    sm.cumE[ab][hh][2] = e2; sm.cumE[ab][hh][3] = e3;
+                pre[hh] = dw ? ar.wtot[hh][0] : 0.f;
+                cum[0][hh] += pre[hh];
+                cum[1][hh] += pre[hh];
+                bend[hh][0] = __shfl_sync(0xffffffffu, cum[1][hh], 15);
+                bend[hh][1] = __shfl_sync(0xffffffffu, cum[1][hh], 31);
+            }
+            const int blk = 2 * dw + (lane >> 4);           // 32-block of tokens 2i, 2i+1
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float cend = (lane >> 4) ? bend[hh][1] : bend[hh][0];
+                const float cbeg = (lane >> 4) ? bend[hh][0] : pre[hh];
+                float vf[2], vd[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float dv = d[e][hh], cv = cum[e][hh];
+                    vf[e] = dv != 0.f ? __expf(cend - cv) * dv : 0.f;
+                    vd[e] = dv != 0.f ? __expf(fminf(cbeg - cv, kDiagFactorLimit)) * dv : 0.f;
+                }
+                *reinterpret_cast<float2 *>(&ar.cum[hh][2 * i]) = make_float2(cum[0][hh], cum[1][hh]);
+                *reinterpret_cast<float2 *>(&ar.dtp[hh][2 * i]) = make_float2(d[0][hh], d[1][hh]);
+                *reinterpret_cast<float2 *>(&ar.vfac[hh][2 * i]) = make_float2(vf[0], vf[1]);
+                *reinterpret_cast<float2 *>(&ar.vdiag[hh][2 * i]) = make_float2(vd[0], vd[1]);
+                if (lane == 15 || lane == 31) {
+                    ar.cumE[hh][blk] = cend;
+                    ar.exact[hh][blk] = fabsf(cend - cbeg) > kDiagFactorLimit;
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.dt_ready[ab]);
-            return true;
-        };
-
-        if (have_cur) ok = dtprep(cur, 0);
-        while (ok && have_cur) {
+            if (lane == 0) mbar_arrive(&sm.arr_ready[ab]);
+            ++kc;
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ===================== Xw and S (lane = token) =====================
+        const int q = warp - 4;
+        const int t = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        Walker wk(&p);
+        Chunk c;
+        uint32_t kc = 0;
+        bool ok = true;
+        while (ok && wk.next(c, false)) {
             const int ab = kc & 1;
-            const int slotX = (3 * kc + 2) % kSlots;
-            const float Dv[2] = {p.D ? p.D[cur.h0] : 0.f, p.D ? p.D[cur.h0 + 1] : 0.f};
-            // ---- S_h from G, in place ----
-            if (!(ok = warp_wait(sm, &sm.dt_ready[ab], (kc >> 1) & 1, status) &&
-                       warp_wait(sm, &sm.g_ready, kc & 1, status)))
+            const Arrays &ar = sm.arr[ab];
+            const uint32_t tX = 3 * kc + 2;
+            const uint8_t *xt = sm.slot[tX % kSlots];
+            // ---- Xw_hi = bf16(w x) into the Xw buffer ----
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status) &&
+                       warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status) &&
+                       (kc == 0 || warp_wait(sm, &sm.xbuf_free, 1, status))))
                 break;
+            const float cum_t0 = ar.cum[0][t], cum_t1 = ar.cum[1][t];
+            const float w0 = (t < c.l) ? __expf(ar.cumE[0][3] - cum_t0) * ar.dtp[0][t] : 0.f;
+            const float w1 = (t < c.l) ? __expf(ar.cumE[1][3] - cum_t1) * ar.dtp[1][t] : 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                    uint4 o;
+                    o.x = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.x), bf16_hi(xv.x))));
+                    o.y = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.y), bf16_hi(xv.y))));
+                    o.z = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.z), bf16_hi(xv.z))));
+                    o.w = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.w), bf16_hi(xv.w))));
+                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = o;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.xhi_ready);
+            // ---- S_h from G, in place ----
+            if (!(ok = warp_wait(sm, &sm.g_ready, kc & 1, status))) break;
             tc_fence_after();
-            const float cum_t[2] = {sm.cum[ab][0][t], sm.cum[ab][1][t]};
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t out0[16], out1[16];
                 if (j > q) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) { out0[i] = 0u; out1[i] = 0u; }
+                    for (int i2 = 0; i2 < 16; ++i2) { out0[i2] = 0u; out1[i2] = 0u; }
                 } else {
                     uint32_t g[32];
                     tmem_ld32(tmem + lane_off + kColG + 32 * j, g);
-                    tmem_wait_ld();
                     if (j < q) {
-                        const float u0 = __expf(cum_t[0] - sm.cumE[ab][0][j]);
-                        const float u1 = __expf(cum_t[1] - sm.cumE[ab][1][j]);
+                        // both factors <= 1: exp(cum_t - cum_e) exp(cum_e - cum_s), cum_e = end of block j
+                        const float u0 = __expf(cum_t0 - ar.cumE[0][j]);
+                        const float u1 = __expf(cum_t1 - ar.cumE[1][j]);
+                        const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int s = 32 * j + 2 * i;
-                            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                            out0[i] = pack_bf16(g0 * u0 * sm.vfac[ab][0][s], g1 * u0 * sm.vfac[ab][0][s + 1]);
-                            out1[i] = pack_bf16(g0 * u1 * sm.vfac[ab][1][s], g1 * u1 * sm.vfac[ab][1][s + 1]);
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const int s = 32 * j + 2 * i2;
+                            const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
+                            const float2 v0 = *reinterpret_cast<const float2 *>(&ar.vfac[0][s]);
+                            const float2 v1 = *reinterpret_cast<const float2 *>(&ar.vfac[1][s]);
+                            out0[i2] = pack2(__fmul2_rn(__fmul2_rn(gg, uu0), v0));
+                            out1[i2] = pack2(__fmul2_rn(__fmul2_rn(gg, uu1), v1));
+                        }
+                    } else if (!ar.exact[0][j] && !ar.exact[1][j]) {
+                        // diagonal block, factored at the block start: exp(cum_t - cum_b) <= 1,
+                        // exp(cum_b - cum_s) <= exp(kDiagFactorLimit)
+                        const float cb0 = j ? ar.cumE[0][j - 1] : 0.f;
+                        const float cb1 = j ? ar.cumE[1][j - 1] : 0.f;
+                        const float u0 = __expf(cum_t0 - cb0), u1 = __expf(cum_t1 - cb1);
+                        const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const int s = 32 * j + 2 * i2;
+                            const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
+                            const float2 v0 = *reinterpret_cast<const float2 *>(&ar.vdiag[0][s]);
+                            const float2 v1 = *reinterpret_cast<const float2 *>(&ar.vdiag[1][s]);
+                            float2 r0 = __fmul2_rn(__fmul2_rn(gg, uu0), v0);
+                            float2 r1 = __fmul2_rn(__fmul2_rn(gg, uu1), v1);
+                            if (s > t) { r0.x = 0.f; r1.x = 0.f; }
+                            if (s + 1 > t) { r0.y = 0.f; r1.y = 0.f; }
+                            out0[i2] = pack2(r0);
+                            out1[i2] = pack2(r1);
                         }
                     } else {
+                        // diagonal block with a steep decay: one exp per element
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int s = 32 * j + 2 * i;
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const int s = 32 * j + 2 * i2;
                             float r0[2], r1[2];
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
-                                const float gv = __uint_as_float(g[2 * i + e]);
+                                const float gv = __uint_as_float(g[2 * i2 + e]);
                                 const bool keep = (s + e) <= t;
-                                r0[e] = keep ? gv * (__expf(cum_t[0] - sm.cum[ab][0][s + e]) * sm.dtp[ab][0][s + e]) : 0.f;
-                                r1[e] = keep ? gv * (__expf(cum_t[1] - sm.cum[ab][1][s + e]) * sm.dtp[ab][1][s + e]) : 0.f;
+                                r0[e] = keep ? gv * (__expf(cum_t0 - ar.cum[0][s + e]) * ar.dtp[0][s + e]) : 0.f;
+                                r1[e] = keep ? gv * (__expf(cum_t1 - ar.cum[1][s + e]) * ar.dtp[1][s + e]) : 0.f;
                             }
-                            out0[i] = pack_bf16(r0[0], r0[1]);
-                            out1[i] = pack_bf16(r1[0], r1[1]);
+                            out0[i2] = pack_bf16(r0[0], r0[1]);
+                            out1[i2] = pack_bf16(r1[0], r1[1]);
                         }
                     }
                 }
                 tmem_st16(tmem + lane_off + kColG + 32 * j, out0);
                 tmem_st16(tmem + lane_off + kColG + 32 * j + 16, out1);
             }
-            const float ecum[2] = {__expf(cum_t[0]), __expf(cum_t[1])};
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.s_ready);
-                mbar_arrive(&sm.arrays_free[ab]);
+                mbar_arrive(&sm.arr_free[ab]);
             }
-            // ---- dt prep of the next block (overlaps the MMAs of this one) ----
-            if (have_nxt && !(ok = dtprep(nxt, kc + 1))) break;
-            // ---- Y *= exp(cum_t) ----
-            if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kColY + 32 * j, r);
-                tmem_wait_ld();
-                const float e = ecum[j >> 1];
+            // ---- Xw_lo = bf16(w x - Xw_hi) once the hi MMA has read the buffer ----
+            if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * e);
-                tmem_st32(tmem + lane_off + kColY + 32 * j, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.y_scaled);
-            // ---- epilogue: y = Y + D x, in place over the X tile ----
-            if (!(ok = warp_wait(sm, &sm.y_ready, kc & 1, status))) break;
-            tc_fence_after();
-            uint8_t *xt = sm.slot[slotX];
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kColY + 32 * j, r);
-                tmem_wait_ld();
-                if (j == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.y_free);
-                }
-                const int hh = j >> 1;
-                uint8_t *row = xt + hh * kHalfBytes + t * 128;
+            for (int hh = 0; hh < 2; ++hh) {
+                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int chunk = (j & 1) * 4 + cc;            // 8 p-values per 16-B chunk
-                    uint4 *ptr = reinterpret_cast<uint4 *>(row + ((chunk ^ (t & 7)) << 4));
-                    const uint4 xv = *ptr;
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                    uint32_t yw[4];
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float y0 = __uint_as_float(r[cc * 8 + 2 * e]) + Dv[hh] * bf16_lo(xw[e]);
-                        const float y1 = __uint_as_float(r[cc * 8 + 2 * e + 1]) + Dv[hh] * bf16_hi(xw[e]);
-                        yw[e] = pack_bf16(y0, y1);
+                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
+                        const uint32_t hi = pack2(v);
+                        o[e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(hi), -bf16_hi(hi))));
                     }
-                    *ptr = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-                }
-            }
-            if (cur.l < kQ && t < cur.l) {
-                // partial block: this row straight to global (a TMA box would overrun
-                // into the next sequence)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint8_t *row = xt + hh * kHalfBytes + t * 128;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out_y) +
-                                                          (cur.row0 + t) * p.H * kP + (cur.h0 + hh) * kP);
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        dst[cc] = *reinterpret_cast<const uint4 *>(row + ((cc ^ (t & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.ytile);
-            if (q == 0) {
-                if (!(ok = warp_wait(sm, &sm.ytile, kc & 1, status))) break;
-                if (lane == 0) {
-                    if (cur.l == kQ) {
-                        const int32_t row = (int32_t)cur.row0;
-                        asm volatile(
-                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                                reinterpret_cast<uint64_t>(&map_y)),
-                            "r"(cur.h0 * kP), "r"(row), "r"(smem_u32(xt))
-                            : "memory");
-                        asm volatile(
-                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                                reinterpret_cast<uint64_t>(&map_y)),
-                            "r"((cur.h0 + 1) * kP), "r"(row), "r"(smem_u32(xt + kHalfBytes))
-                            : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    }
-                    mbar_arrive(&sm.empty[slotX]);
-                }
-                __syncwarp();
-            }
-            cur = nxt;
-            have_cur = have_nxt;
-            if (have_cur) have_nxt = wk.next(nxt, false);
+            if (lane == 0) mbar_arrive(&sm.xlo_ready);
             ++kc;
         }
-        if (q == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    } else if (warp >= 8) {
-        // ===================== state warpgroups =====================
-        const int wg = (warp - 8) >> 2;          // n half: columns [64 wg, 64 wg + 64)
-        const int q = warp & 3;
-        const int r = q * 32 + lane;             // head * 64 + p
-        const int hh = r >> 6, pp = r & 63;
+    } else if (warp >= 8 && warp < 12) {
+        // ===================== epilogue (lane = token) =====================
+        const int q = warp - 8;
+        const int t = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         Walker wk(&p);
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
-        float h[64];
-        StT *cache = static_cast<StT *>(p.state_cache);
-        uint8_t *hrow = sm.hbuf[wg] + r * 128;
-        while (ok && wk.next(c, true)) {
-            const int64_t srow = ((int64_t)c.slot * p.H + c.h0 + hh) * (kP * kN) + pp * kN + wg * 64;
-            if (c.first) {
-                if (c.init) {
-                    load_state_row<StT>(cache + srow, h);
-                } else {
+        __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.out_y);
+        while (ok && wk.next(c, false)) {
+            const int ab = kc & 1;
+            const uint32_t ycol = kColY + 128 * (kc & 1);
+            const uint8_t *xt = sm.slot[(3 * kc + 2) % kSlots];
+            // ---- Y[b] *= exp(cum_t) ----
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
+            const float e0 = __expf(sm.arr[ab].cum[0][t]), e1 = __expf(sm.arr[ab].cum[1][t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
+            if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
+            tc_fence_after();
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) h[i] = 0.f;
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
+                tmem_wait_ld();
+                const float2 ee = (j >> 1) ? make_float2(e1, e1) : make_float2(e0, e0);
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const float2 v = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ee);
+                    r[2 * i2] = __float_as_uint(v.x);
+                    r[2 * i2 + 1] = __float_as_uint(v.y);
+                }
+                tmem_st32(tmem + lane_off + ycol + 32 * j, r);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.y_scaled);
+            // ---- y = Y + D x (x from the smem tile, which stays until x_epi_done) ----
+            const bool valid = t < c.l;
+            const int64_t grow = (c.row0 + t) * (int64_t)p.H * kP + (int64_t)c.h0 * kP;
+            const float D0 = p.D ? p.D[c.h0] : 0.f, D1 = p.D ? p.D[c.h0 + 1] : 0.f;
+            if (!(ok = warp_wait(sm, &sm.y_ready, kc & 1, status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
+                tmem_wait_ld();
+                if (j == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.y_free[kc & 1]);
+                }
+                const int hh = j >> 1;
+                const float2 dd = hh ? make_float2(D1, D1) : make_float2(D0, D0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int chunk = (j & 1) * 4 + cc;
+                    const uint4 x4 = *reinterpret_cast<const uint4 *>(
+                        xt + hh * kHalfBytes + t * 128 + ((chunk ^ (t & 7)) << 4));
+                    const uint32_t xw4[4] = {x4.x, x4.y, x4.z, x4.w};
+                    uint32_t yw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        yw[e] = pack2(__ffma2_rn(dd, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])),
+                                                 f2(r[cc * 8 + 2 * e], r[cc * 8 + 2 * e + 1])));
+                    if (valid)
+                        reinterpret_cast<uint4 *>(yg + grow)[j * 4 + cc] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.x_epi_done[kc & 1]);
+            ++kc;
+        }
+    } else {
+        // ===================== state (lane = state column n) =====================
+        // Warps 12-13 own n < 64, warps 14-15 n >= 64; C h^T is split the same way
+        // along n, so the bf16 copy of h needs only one half-size buffer.
+        const int q = warp - 12;
+        const int n = q * 32 + lane;
+        const bool first_half = q < 2;
+        const int hrow = n & 63;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        Walker wk(&p);
+        Chunk c;
+        uint32_t kc = 0;
+        bool ok = true;
+        StT *cache = static_cast<StT *>(p.state_cache);
+        // bf16 copy of 32 state values (head j/2, p block j%2) into this lane's hbuf row
+        auto put_hbuf = [&](int j, const uint32_t (&w)[16]) {
+            uint8_t *rowp = sm.hbuf + (j >> 1) * kHbufHead + hrow * 128;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int chunk = (j & 1) * 4 + cc;
+                *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (hrow & 7)) << 4)) =
+                    make_uint4(w[cc * 4], w[cc * 4 + 1], w[cc * 4 + 2], w[cc * 4 + 3]);
+            }
+        };
+        while (ok && wk.next(c, true)) {
+            const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
             if (c.empty_item) {
-                if (p.write_final) store_state_row<StT>(cache + srow, h);
+                if (p.write_final) {
+                    for (int col = 0; col < 2 * kP; ++col) {
+                        const float v = c.init ? load_state<StT>(cache + hbase + (int64_t)col * kN) : 0.f;
+                        store_state<StT>(cache + hbase + (int64_t)col * kN, v);
+                    }
+                }
                 continue;
             }
-            if (c.first) {
-                // state entering block 0 of the item -> hbuf for Y = C h^T
-                if (kc > 0 && !(ok = warp_wait(sm, &sm.yinter_ready, (kc - 1) & 1, status))) break;
-                write_hbuf_row(hrow, r, h);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.hs_ready);
+            // Entering block kc: the state source is the cache slot (first block of the
+            // item) or the TMEM accumulator after block kc-1.  Each lane writes its bf16
+            // copy into hbuf once C h^T may overwrite it (first half of n after the
+            // previous block's C h^T, second half after this block's first-half C h^T),
+            // and stores state * exp(cum_end of block kc) back into TMEM.
+            const bool from_cache = c.first;
+            if (!from_cache) {
+                // wait for this block's predecessor to finish its state MMAs
+                if (!(ok = warp_wait(sm, &sm.state_done, (kc - 1) & 1, status))) break;
+                tc_fence_after();
             }
-            // ---- Xw^T (hi, lo) of this block into TMEM ----
             const int ab = kc & 1;
-            const uint32_t tx = 3 * kc + 2;
-            if (!(ok = warp_wait(sm, &sm.full[tx % kSlots], (tx / kSlots) & 1, status) &&
-                       warp_wait(sm, &sm.dt_ready[ab], (kc >> 1) & 1, status) &&
-                       (kc == 0 || warp_wait(sm, &sm.sc_ready, (kc - 1) & 1, status))))
-                break;
-            tc_fence_after();
-            {
-                const uint8_t *xt = sm.slot[tx % kSlots] + hh * kHalfBytes;
-                const int chunk = pp >> 3, within = (pp & 7) * 2;
-#pragma unroll 1
-                for (int grp = 0; grp < 4; ++grp) {
-                    uint32_t whi[8], wlo[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float v[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int s = wg * 64 + grp * 16 + 2 * i + e;
-                            const uint16_t xb = *reinterpret_cast<const uint16_t *>(
-                                xt + s * 128 + ((chunk ^ (s & 7)) << 4) + within);
-                            const float wv = sm.wfac[ab][hh][s];
-                            v[e] = (wv != 0.f) ? wv * __uint_as_float((uint32_t)xb << 16) : 0.f;
-                        }
-                        whi[i] = pack_bf16(v[0], v[1]);
-                        wlo[i] = pack_bf16(v[0] - bf16_lo(whi[i]), v[1] - bf16_hi(whi[i]));
-                    }
-                    const uint32_t col = wg * 32 + grp * 8;
-                    tmem_st8(tmem + lane_off + kColXhi + col, whi);
-                    tmem_st8(tmem + lane_off + kColXlo + col, wlo);
-                }
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
+            const float2 dd0 = make_float2(__expf(sm.arr[ab].cumE[0][3]), __expf(sm.arr[ab].cumE[0][3]));
+            const float2 dd1 = make_float2(__expf(sm.arr[ab].cumE[1][3]), __expf(sm.arr[ab].cumE[1][3]));
+            if (first_half) {
+                if (kc > 0 && !(ok = warp_wait(sm, &sm.yinter_ready, (kc - 1) & 1, status))) break;
+            } else {
+                if (!(ok = warp_wait(sm, &sm.hbuf_a_done, kc & 1, status))) break;
             }
-            const float delta = sm.cumE[ab][hh][3];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                if (from_cache) {
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; ++i2)
+                        r[i2] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 32 + i2) * kN) : 0.f);
+                } else {
+                    tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
+                    tmem_wait_ld();
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const float2 v = f2(r[2 * i2], r[2 * i2 + 1]);
+                    w[i2] = pack2(v);
+                    const float2 sv = __fmul2_rn(v, (j >> 1) ? dd1 : dd0);
+                    r[2 * i2] = __float_as_uint(sv.x);
+                    r[2 * i2 + 1] = __float_as_uint(sv.y);
+                }
+                put_hbuf(j, w);
+                tmem_st32(tmem + lane_off + kColH + 32 * j, r);
+            }
+            fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sm.xp_ready);
-                mbar_arrive(&sm.arrays_free[ab]);
-            }
-            // ---- state update: h = exp(cum_end) h + Sc ----
-            if (!(ok = warp_wait(sm, &sm.sc_ready, kc & 1, status))) break;
-            tc_fence_after();
-            {
-                uint32_t s0[32], s1[32];
-                tmem_ld32(tmem + lane_off + kColSc + wg * 64, s0);
-                tmem_ld32(tmem + lane_off + kColSc + wg * 64 + 32, s1);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.sc_free);
-                const float dec = __expf(delta);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    h[i] = fmaf(dec, h[i], __uint_as_float(s0[i]));
-                    h[32 + i] = fmaf(dec, h[32 + i], __uint_as_float(s1[i]));
-                }
+                mbar_arrive(first_half ? &sm.hs_a : &sm.hs_b);
+                mbar_arrive(&sm.state_ready);
+                mbar_arrive(&sm.arr_free[ab]);
             }
             if (c.last) {
-                if (p.write_final) store_state_row<StT>(cache + srow, h);
-            } else {
-                if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
-                write_hbuf_row(hrow, r, h);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.hs_ready);
+                // final state of the item, straight from the accumulator
+                if (!(ok = warp_wait(sm, &sm.state_done, kc & 1, status))) break;
+                tc_fence_after();
+                if (p.write_final) {
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i2 = 0; i2 < 32; ++i2)
+                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + i2) * kN, __uint_as_float(r[i2]));
+                    }
+                }
+                tc_fence_before();
             }
             ++kc;
         }
@@ -896,9 +960,8 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStr
         }
         sms = di.sms;
     }
-    CUtensorMap mx, mb, mc, my;
+    CUtensorMap mx, mb, mc;
     if (!make_map(&mx, a.x, (uint64_t)a.H * kP, (uint64_t)a.T) ||
-        !make_map(&my, a.out_y, (uint64_t)a.H * kP, (uint64_t)a.T) ||
         !make_map(&mb, a.B, (uint64_t)a.G * kN, (uint64_t)a.T) ||
         !make_map(&mc, a.C, (uint64_t)a.G * kN, (uint64_t)a.T))
         return cudaErrorInvalidValue;
@@ -927,9 +990,10 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStr
     p.has_init = a.has_init;
     p.state_cache = a.state_cache;
     p.out_y = a.out_y;
+    p.x = a.x;
     p.device_status = a.device_status;
     const int grid = p.num_items < sms ? p.num_items : sms;
-    chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, my, p);
+    chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
     return cudaGetLastError();
 }
 
