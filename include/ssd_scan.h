@@ -71,7 +71,9 @@ typedef enum {
     SSD_ERR_INVALID_ARG = 1,  /* bad size, NULL required pointer, bad dtype */
     SSD_ERR_UNSUPPORTED = 2,  /* valid but not compiled (e.g. dstate > 256) */
     SSD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required   */
-    SSD_ERR_CUDA = 4          /* a CUDA runtime/driver call failed          */
+    SSD_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed          */
+    SSD_ERR_SCRATCH_LIMIT = 5 /* batch larger than the fixed scratch of
+                                 ssd_scan_varlen_noalloc                    */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype;
@@ -137,6 +139,30 @@ int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params);
  * scan), "recurrent" (token-by-token SIMT scan: fp32 I/O, intermediate
  * states, continuations of at most 3 tokens, other shapes) or "invalid". */
 const char *ssd_scan_varlen_path(const ssd_scan_params *params);
+
+/* Maximum number of sequences ssd_scan_varlen_noalloc accepts. */
+#define SSD_NOALLOC_MAX_SEQS 65536
+
+/* The same scan as ssd_scan_varlen for callers that cannot allocate device
+ * memory (the pages have no counterpart: this is a library convenience).
+ * Examples: an engine that hands all free HBM to its state and KV pools and
+ * allows no later cudaMalloc, a plug-in ABI that only passes the caller's own
+ * tensors, or a latency-critical path that cannot afford cudaMalloc's
+ * device-wide synchronisation.  Instead of params->workspace (ignored here)
+ * the scratch comes from a fixed array in the library's device memory, so
+ * the call itself allocates nothing and calls no allocating routine.
+ *   - Limit: num_seqs <= SSD_NOALLOC_MAX_SEQS, else SSD_ERR_SCRATCH_LIMIT and
+ *     nothing is enqueued.  Every GPU that loads the library keeps the
+ *     array (256 KiB) until the process exits.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array.  Calls whose kernels may overlap on the GPU
+ *     (unordered streams) race on it; order them on one stream or use
+ *     ssd_scan_varlen with separate workspaces.  Nothing in the array needs
+ *     to start zeroed: each call rewrites what it reads.
+ * Everything else (arguments, aliasing, errors, results) is as for
+ * ssd_scan_varlen. */
+ssd_status ssd_scan_varlen_noalloc(const ssd_scan_params *params, struct CUstream_st *stream);
 
 /* Static description of a status code. */
 const char *ssd_status_string(ssd_status status);

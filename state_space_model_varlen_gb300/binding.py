@@ -13,13 +13,15 @@ from typing import Optional
 
 from . import _build
 
-SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA = range(5)
+(SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA,
+ SSD_ERR_SCRATCH_LIMIT) = range(6)
+SSD_NOALLOC_MAX_SEQS = 65536
 SSD_F32, SSD_BF16, SSD_F16 = 0, 1, 2
 SSD_DEV_BAD_SLOT, SSD_DEV_BAD_SEQLENS = 1, 2
 
 # every exported entry point declared in include/ssd_scan.h
 EXPORTED = ("ssd_scan_varlen", "ssd_scan_varlen_workspace_size", "ssd_scan_varlen_num_launches",
-            "ssd_scan_varlen_path", "ssd_status_string")
+            "ssd_scan_varlen_path", "ssd_status_string", "ssd_scan_varlen_noalloc")
 
 
 class ScanParams(ctypes.Structure):
@@ -86,6 +88,8 @@ def load(build_if_missing: bool = True):
             lib.ssd_scan_varlen_num_launches.argtypes = [P]
             lib.ssd_scan_varlen_path.restype = ctypes.c_char_p
             lib.ssd_scan_varlen_path.argtypes = [P]
+            lib.ssd_scan_varlen_noalloc.restype = ctypes.c_int
+            lib.ssd_scan_varlen_noalloc.argtypes = [P, ctypes.c_void_p]
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -183,6 +187,14 @@ def kernel_path(params: ScanParams) -> str:
 
 def call(params: ScanParams, stream_ptr: int = 0) -> None:
     rc = load().ssd_scan_varlen(ctypes.byref(params), ctypes.c_void_p(stream_ptr or None))
+    if rc != SSD_OK:
+        raise SSDError(rc)
+
+
+def call_noalloc(params: ScanParams, stream_ptr: int = 0) -> None:
+    """``ssd_scan_varlen_noalloc``: the scan with the library's fixed scratch
+    instead of ``params.workspace`` (for callers that cannot allocate)."""
+    rc = load().ssd_scan_varlen_noalloc(ctypes.byref(params), ctypes.c_void_p(stream_ptr or None))
     if rc != SSD_OK:
         raise SSDError(rc)
 

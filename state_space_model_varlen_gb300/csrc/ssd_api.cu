@@ -4,9 +4,12 @@
 
 #include "ssd_internal.h"
 
-namespace {
+namespace ssd {
+namespace detail {
 
+namespace {
 bool dtype_ok(int d) { return d == SSD_F32 || d == SSD_BF16 || d == SSD_F16; }
+}  // namespace
 
 // Host-side argument validation; no device memory is read.
 ssd_status validate(const ssd_scan_params *p) {
@@ -70,7 +73,12 @@ bool use_chunked(const ssd_scan_params *p) {
     return ssd::chunked_supported(*p);
 }
 
-}  // namespace
+}  // namespace detail
+}  // namespace ssd
+
+using ssd::detail::make_args;
+using ssd::detail::use_chunked;
+using ssd::detail::validate;
 
 extern "C" {
 
@@ -116,6 +124,7 @@ const char *ssd_status_string(ssd_status status) {
         case SSD_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case SSD_ERR_CUDA: return "CUDA error while enqueueing";
+        case SSD_ERR_SCRATCH_LIMIT: return "batch exceeds the fixed scratch of the no-allocation entry point";
     }
     return "unknown status";
 }

@@ -34,4 +34,12 @@ size_t chunked_workspace_bytes(const ssd_scan_params &p);
 cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace,
                            cudaStream_t stream);
 
+namespace detail {
+// Host-side argument checks, launch arguments and kernel-path choice shared by
+// the entry points (defined in ssd_api.cu).
+ssd_status validate(const ssd_scan_params *p);
+ScanArgs make_args(const ssd_scan_params *p);
+bool use_chunked(const ssd_scan_params *p);
+}  // namespace detail
+
 }  // namespace ssd
