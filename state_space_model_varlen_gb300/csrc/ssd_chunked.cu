@@ -29,18 +29,21 @@
 //   fp32 accumulation.  Y is double buffered in TMEM so block k+1's C h^T can
 //   start while block k's epilogue drains.
 //
-// Warp roles (16 warps): warp 0 TMA producer, warp 1 MMA issuer, warps 2-3 dt
-// softplus + within-block cumsum (running a block ahead), warps 4-7 "Xw/S"
-// (lane = token), warps 8-11 "epilogue" (lane = token: row scaling, y = Y + D x,
-// stores), warps 12-15 "state" (lane = state column n: state in TMEM, bf16
-// copy for C h^T, per-block decay, cache I/O).  All hand-offs are mbarriers;
-// every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT in
-// device_status instead of hanging.
+// Warp roles (16 warps): warp 0 TMA producer; warp 1 issues the output-path
+// MMAs (G, C h^T, S X) and warp 3 the state-path MMAs (B^T Xw), so neither
+// path waits behind the other; warp 2 owns the TMEM allocation; warps 4-7
+// (lane = token) compute dt softplus, the within-block cumsum and the state
+// scales a block ahead and build the scaled Xw; warps 8-11 build S, scale the
+// rows of Y and write y (lane = token); warps 12-15 own the state (lane = state column n: bf16 copy for
+// C h^T, occasional renormalisation, cache I/O).  All hand-offs are
+// mbarriers; every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT
+// in device_status instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "sm100.cuh"
@@ -58,10 +61,11 @@ constexpr int kSlots = 5;          // TMA ring of 32 KB tiles (C, B, X per block
 constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kHbufHead = 8192;    // one head of the half-n bf16 state copy: 64 rows x 128 B
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;     // 16 warps, each with exactly one role below
 constexpr uint64_t kSpinLimit = 4000000000ull;   // clock cycles (~2 s) per wait
 constexpr float kDiagFactorLimit = 80.f;         // |decay| of a 32-token block for the
                                                  // factored diagonal path (e^80 < fp32 max)
+constexpr float kScaleLimit = 80.f;              // |exponent| bound of the scaled state inputs
 
 // TMEM columns
 constexpr uint32_t kColG = 0;      // G / S (in place), lanes = tokens
@@ -85,15 +89,30 @@ struct Params {
     int32_t *device_status;
 };
 
-// per-block decay arrays, written by the dt warps
-struct Arrays {
+// per-block decay arrays, written by the Xw warps a block ahead
+//
+// The state is accumulated in TMEM in a scaled form hs = h exp(-R): a block
+// adds B^T (exp(E - cum_s) dt'_s x_s) with E = -R' and R' the scale in force
+// for the block, so no per-block rescale of the accumulator is needed.  R'
+// keeps the running scale (R' = R_prev, "fast") while every exponent of the
+// block stays within +-kScaleLimit; otherwise the accumulator is renormalised
+// to exp(dlt) h before the block (R' = -dlt, exponents <= 0).  After the block
+// R = R' + dlt, with dlt the block's total decay cum_end.
+struct __align__(16) Arrays {
     float cum[2][kQ];      // [head][token] within-block cumsum of dt' A
     float dtp[2][kQ];      // dt'
     float vfac[2][kQ];     // exp(cum at end of s's 32-block - cum_s) dt'_s
     float vdiag[2][kQ];    // exp(cum before s's 32-block - cum_s) dt'_s
     float cumE[2][4];      // cum at the end of each 32-token block
-    float wtot[2][2];      // scan scratch [head][dt warp]
+    float E[2];            // exponent base of the scaled Xw for this block
+    float eprev[2];        // exp(R_prev): hs before the block -> h
+    float edlt[2];         // exp(dlt)
+    float eend[2];         // exp(R after the block): hs after the block -> h
+    int32_t renorm[2];     // renormalise the accumulator before this block
     int32_t exact[2][4];   // diagonal block needs the per-element path
+    float wtot[2][4];      // per 32-token block: sum of dt' A
+    float wmin[2][4];      // per 32-token block: extremes of its local cumsum
+    float wmax[2][4];
 };
 
 struct __align__(1024) Smem {
@@ -102,14 +121,22 @@ struct __align__(1024) Smem {
     uint8_t hbuf[2 * kHbufHead];          // bf16 h, one half of n at a time: [head][n % 64][p]
     Arrays arr[2];
     uint64_t full[kSlots], empty[kSlots];
-    uint64_t arr_ready[2], arr_free[2], dt_scan[2];
+    uint64_t arr_ready[2], arr_free[2], scan_bar[2];
     uint64_t g_ready, s_ready, xhi_ready, xlo_ready, xbuf_free;
-    uint64_t hs_a, hs_b, hbuf_a_done, state_ready, state_done;
+    uint64_t hs_a, hs_b, hbuf_a_done, state_ok, state_done;
     uint64_t yinter_ready, y_scaled, y_ready, y_free[2], x_epi_done[2];
-    uint64_t drain;
+    uint64_t drain_y, drain_h;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
+
+// Vector (8/16-byte) shared-memory accesses rely on these offsets.
+static_assert(sizeof(Arrays) % 16 == 0, "Arrays must keep float4 rows aligned");
+static_assert(offsetof(Arrays, dtp) % 16 == 0 && offsetof(Arrays, vfac) % 16 == 0 &&
+              offsetof(Arrays, vdiag) % 16 == 0, "Arrays rows must be 16-byte aligned");
+static_assert(offsetof(Smem, arr) % 16 == 0, "Arrays must start 16-byte aligned");
+static_assert(offsetof(Smem, xw) % 1024 == 0 && offsetof(Smem, hbuf) % 1024 == 0,
+              "swizzled operand tiles must be 1024-byte aligned");
 
 // ---------------------------------------------------------------------------
 // work enumeration, identical in every role
@@ -320,12 +347,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
+        for (int i = 0; i < kSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 2); }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.arr_ready[i], 2);
+            mbar_init(&sm.arr_ready[i], 4);
+            mbar_init(&sm.scan_bar[i], 4);
             mbar_init(&sm.arr_free[i], 12);
-            mbar_init(&sm.dt_scan[i], 2);
             mbar_init(&sm.y_free[i], 4);
+            mbar_init(&sm.x_epi_done[i], 4);
         }
         mbar_init(&sm.g_ready, 1);
         mbar_init(&sm.s_ready, 4);
@@ -335,14 +363,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         mbar_init(&sm.hs_a, 2);
         mbar_init(&sm.hs_b, 2);
         mbar_init(&sm.hbuf_a_done, 1);
-        mbar_init(&sm.state_ready, 4);
+        mbar_init(&sm.state_ok, 4);
         mbar_init(&sm.state_done, 1);
         mbar_init(&sm.yinter_ready, 1);
         mbar_init(&sm.y_scaled, 4);
         mbar_init(&sm.y_ready, 1);
-        mbar_init(&sm.x_epi_done[0], 4);
-        mbar_init(&sm.x_epi_done[1], 4);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain_y, 1);
+        mbar_init(&sm.drain_h, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -396,14 +423,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 wait_bar(sm, &sm.full[t % kSlots], (t / kSlots) & 1, nullptr);
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer =====================
+        // ===================== MMA issuer, output path =====================
         if (lane == 0) {
             Walker wk(&p);
             Chunk c;
             uint32_t kc = 0;
             bool ok = true;
             const uint32_t bH = smem_u32(sm.hbuf);
-            const uint32_t bW = smem_u32(sm.xw[0]);
             while (ok && wk.next(c, false)) {
                 const uint32_t tC = 3 * kc, tB = 3 * kc + 1, tX = 3 * kc + 2;
                 const uint32_t bC = smem_u32(sm.slot[tC % kSlots]);
@@ -422,6 +448,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            smem_desc_sw128(bB + off, 16, 1024), kIdG, ks > 0);
                 }
                 mma_commit(&sm.g_ready);
+                mma_commit(&sm.empty[tB % kSlots]);              // this path's only read of B
                 // ---- Y[b] = C h^T, first half of the state columns n ----
                 if (!(ok = wait_bar(sm, &sm.hs_a, kc & 1, status) &&
                            (kc < 2 || wait_bar(sm, &sm.y_free[kc & 1], ((kc >> 1) - 1) & 1, status))))
@@ -432,16 +459,6 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                     mma_ss(tmem + ycol, smem_desc_sw128(bC + ks * 32, 16, 1024),
                            smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, ks > 0);
                 mma_commit(&sm.hbuf_a_done);
-                // ---- h += B^T Xw_hi ----
-                if (!(ok = wait_bar(sm, &sm.xhi_ready, kc & 1, status) &&
-                           wait_bar(sm, &sm.state_ready, kc & 1, status)))
-                    break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
-                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
-                mma_commit(&sm.xbuf_free);
                 // ---- Y[b] += C h^T, second half of n ----
                 if (!(ok = wait_bar(sm, &sm.hs_b, kc & 1, status))) break;
                 tc_fence_after();
@@ -450,6 +467,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                     mma_ss(tmem + ycol, smem_desc_sw128(bC + kHalfBytes + ks * 32, 16, 1024),
                            smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, 1);
                 mma_commit(&sm.yinter_ready);
+                mma_commit(&sm.empty[tC % kSlots]);
                 mma_commit(&sm.empty[tC % kSlots]);
                 // ---- Y[b] += S_h X_h ----
                 if (!(ok = wait_bar(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status) &&
@@ -467,7 +485,35 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                     }
                 }
                 mma_commit(&sm.y_ready);
-                // ---- h += B^T Xw_lo ----
+                mma_commit(&sm.empty[tX % kSlots]);
+                ++kc;
+            }
+            mma_commit(&sm.drain_y);
+            wait_bar(sm, &sm.drain_y, 0, nullptr);
+        }
+    } else if (warp == 3) {
+        // ===================== MMA issuer, state path =====================
+        if (lane == 0) {
+            Walker wk(&p);
+            Chunk c;
+            uint32_t kc = 0;
+            bool ok = true;
+            const uint32_t bW = smem_u32(sm.xw[0]);
+            while (ok && wk.next(c, false)) {
+                const uint32_t tB = 3 * kc + 1, tX = 3 * kc + 2;
+                const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
+                // ---- hs += B^T Xw_hi ----
+                if (!(ok = wait_bar(sm, &sm.full[tB % kSlots], (tB / kSlots) & 1, status) &&
+                           wait_bar(sm, &sm.xhi_ready, kc & 1, status) &&
+                           wait_bar(sm, &sm.state_ok, kc & 1, status)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
+                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
+                mma_commit(&sm.xbuf_free);
+                // ---- hs += B^T Xw_lo ----
                 if (!(ok = wait_bar(sm, &sm.xlo_ready, kc & 1, status))) break;
                 tc_fence_after();
 #pragma unroll
@@ -477,111 +523,159 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 mma_commit(&sm.state_done);
                 mma_commit(&sm.xbuf_free);
                 mma_commit(&sm.empty[tB % kSlots]);
-                mma_commit(&sm.empty[tX % kSlots]);     // the Xw passes have read X by now
+                mma_commit(&sm.empty[tX % kSlots]);              // the Xw passes have read X
                 ++kc;
             }
-            mma_commit(&sm.drain);
-            wait_bar(sm, &sm.drain, 0, nullptr);
+            mma_commit(&sm.drain_h);
+            wait_bar(sm, &sm.drain_h, 0, nullptr);
         }
-    } else if (warp == 2 || warp == 3) {
-        // ===================== dt softplus + cumsum (a block ahead) =====================
-        const int dw = warp - 2;
-        const int i = dw * 32 + lane;             // tokens 2i, 2i+1
+    } else if (warp == 2) {
+        // TMEM owner only: allocates above, frees after the final barrier
+    } else if (warp >= 4 && warp < 8) {
+        // ===================== dt, scales and the scaled Xw (lane = token) =====================
+        // Per block k (once X lands): the dt arrays of block k+1, the lo part of
+        // Xw into registers, the hi part into the Xw buffer once block k-1's
+        // state MMAs have read it, the lo part once the hi MMA has read it.  Only
+        // the two buffer fills sit on the state recurrence's critical path.
+        const int q = warp - 4;
+        const int t = q * 32 + lane;
         Walker wk(&p);
         Chunk c;
+        bool have_cur = wk.next(c, false);
+        int32_t cur_l = c.l;                      // valid tokens of the block being filled
         uint32_t kc = 0;
-        while (wk.next(c, false)) {
-            const int ab = kc & 1;
+        bool ok = true;
+        float R0 = 0.f, R1 = 0.f;                 // running scale of the state accumulator
+
+        // dt softplus, within-block cumsum and the per-block scales of block k
+        auto dtprep = [&](const Chunk &c, uint32_t k) -> bool {
+            const int ab = k & 1;
             Arrays &ar = sm.arr[ab];
-            if (kc >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((kc >> 1) - 1) & 1, status)) break;
-            float d[2][2] = {{0.f, 0.f}, {0.f, 0.f}};       // [token][head]
-            const float bias0 = p.dt_bias ? p.dt_bias[c.h0] : 0.f;
-            const float bias1 = p.dt_bias ? p.dt_bias[c.h0 + 1] : 0.f;
-            const float A0 = p.A[c.h0], A1 = p.A[c.h0 + 1];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tok = 2 * i + e;
-                if (tok < c.l) {
-                    const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (c.row0 + tok) * p.H + c.h0);
-                    const float z0 = raw.x + bias0, z1 = raw.y + bias1;
-                    d[e][0] = p.dt_softplus ? softplus_f(z0) : z0;
-                    d[e][1] = p.dt_softplus ? softplus_f(z1) : z1;
-                }
+            if (k >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((k >> 1) - 1) & 1, status)) return false;
+            if (c.first) { R0 = 0.f; R1 = 0.f; }
+            float d0 = 0.f, d1 = 0.f;
+            if (t < c.l) {
+                const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (c.row0 + t) * p.H + c.h0);
+                const float z0 = raw.x + (p.dt_bias ? p.dt_bias[c.h0] : 0.f);
+                const float z1 = raw.y + (p.dt_bias ? p.dt_bias[c.h0 + 1] : 0.f);
+                d0 = p.dt_softplus ? softplus_f(z0) : z0;
+                d1 = p.dt_softplus ? softplus_f(z1) : z1;
             }
-            float cum[2][2];                              // [token][head]
+            float s0 = d0 * p.A[c.h0], s1 = d1 * p.A[c.h0 + 1];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float Ah = hh ? A1 : A0;
-                const float a0 = d[0][hh] * Ah, a1 = d[1][hh] * Ah;
-                float s = a0 + a1;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v0 = __shfl_up_sync(0xffffffffu, s0, off);
+                const float v1 = __shfl_up_sync(0xffffffffu, s1, off);
+                if (lane >= off) { s0 += v0; s1 += v1; }
+            }
+            // warp extremes of the local scan (the block's cum range follows from them)
+            float mn0 = s0, mx0 = s0, mn1 = s1, mx1 = s1;
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float v = __shfl_up_sync(0xffffffffu, s, off);
-                    if (lane >= off) s += v;
-                }
-                cum[1][hh] = s;
-                cum[0][hh] = s - a1;
-                if (lane == 31) ar.wtot[hh][dw] = s;
+            for (int off = 16; off > 0; off >>= 1) {
+                mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, off));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            if (lane == 31) {
+                ar.wtot[0][q] = s0; ar.wtot[1][q] = s1;
+                ar.wmin[0][q] = mn0; ar.wmin[1][q] = mn1;
+                ar.wmax[0][q] = mx0; ar.wmax[1][q] = mx1;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.dt_scan[ab]);
-            if (!warp_wait(sm, &sm.dt_scan[ab], (kc >> 1) & 1, status)) break;
-            float pre[2], bend[2][2];                     // cum at the end of this warp's two 32-blocks
+            if (lane == 0) mbar_arrive(&sm.scan_bar[ab]);
+            if (!warp_wait(sm, &sm.scan_bar[ab], (k >> 1) & 1, status)) return false;
+            float cE[2][4], lo[2], hi[2];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                pre[hh] = dw ? ar.wtot[hh][0] : 0.f;
-                cum[0][hh] += pre[hh];
-                cum[1][hh] += pre[hh];
-                bend[hh][0] = __shfl_sync(0xffffffffu, cum[1][hh], 15);
-                bend[hh][1] = __shfl_sync(0xffffffffu, cum[1][hh], 31);
+                float run = 0.f;
+                lo[hh] = 0.f;
+                hi[hh] = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    lo[hh] = fminf(lo[hh], run + ar.wmin[hh][w]);
+                    hi[hh] = fmaxf(hi[hh], run + ar.wmax[hh][w]);
+                    run += ar.wtot[hh][w];
+                    cE[hh][w] = run;
+                }
             }
-            const int blk = 2 * dw + (lane >> 4);           // 32-block of tokens 2i, 2i+1
+            // cum before and at the end of this warp's 32-token block (static indices only)
+            float pre0 = 0.f, pre1 = 0.f, end0 = cE[0][0], end1 = cE[1][0];
+#pragma unroll
+            for (int w = 1; w < 4; ++w)
+                if (q == w) { pre0 = cE[0][w - 1]; pre1 = cE[1][w - 1]; end0 = cE[0][w]; end1 = cE[1][w]; }
+            const float c0 = s0 + pre0, c1 = s1 + pre1;
+            ar.cum[0][t] = c0;
+            ar.cum[1][t] = c1;
+            ar.dtp[0][t] = d0;
+            ar.dtp[1][t] = d1;
+            ar.vfac[0][t] = d0 != 0.f ? __expf(end0 - c0) * d0 : 0.f;
+            ar.vfac[1][t] = d1 != 0.f ? __expf(end1 - c1) * d1 : 0.f;
+            ar.vdiag[0][t] = d0 != 0.f ? __expf(fminf(pre0 - c0, kDiagFactorLimit)) * d0 : 0.f;
+            ar.vdiag[1][t] = d1 != 0.f ? __expf(fminf(pre1 - c1, kDiagFactorLimit)) * d1 : 0.f;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float cend = (lane >> 4) ? bend[hh][1] : bend[hh][0];
-                const float cbeg = (lane >> 4) ? bend[hh][0] : pre[hh];
-                float vf[2], vd[2];
+                float &R = hh ? R1 : R0;
+                const float dlt = cE[hh][3];
+                const bool fast = (-R - lo[hh] <= kScaleLimit) && (-R - hi[hh] >= -kScaleLimit);
+                const float Rp = fast ? R : -dlt;          // scale in force for this block
+                if (t == 0) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float dv = d[e][hh], cv = cum[e][hh];
-                    vf[e] = dv != 0.f ? __expf(cend - cv) * dv : 0.f;
-                    vd[e] = dv != 0.f ? __expf(fminf(cbeg - cv, kDiagFactorLimit)) * dv : 0.f;
+                    for (int j = 0; j < 4; ++j) {
+                        ar.cumE[hh][j] = cE[hh][j];
+                        const float cb = j ? cE[hh][j - 1] : 0.f;
+                        ar.exact[hh][j] = fabsf(cE[hh][j] - cb) > kDiagFactorLimit;
+                    }
+                    ar.E[hh] = -Rp;
+                    ar.eprev[hh] = __expf(R);
+                    ar.edlt[hh] = __expf(dlt);
+                    ar.eend[hh] = __expf(Rp + dlt);
+                    ar.renorm[hh] = fast ? 0 : 1;
                 }
-                *reinterpret_cast<float2 *>(&ar.cum[hh][2 * i]) = make_float2(cum[0][hh], cum[1][hh]);
-                *reinterpret_cast<float2 *>(&ar.dtp[hh][2 * i]) = make_float2(d[0][hh], d[1][hh]);
-                *reinterpret_cast<float2 *>(&ar.vfac[hh][2 * i]) = make_float2(vf[0], vf[1]);
-                *reinterpret_cast<float2 *>(&ar.vdiag[hh][2 * i]) = make_float2(vd[0], vd[1]);
-                if (lane == 15 || lane == 31) {
-                    ar.cumE[hh][blk] = cend;
-                    ar.exact[hh][blk] = fabsf(cend - cbeg) > kDiagFactorLimit;
-                }
+                R = Rp + dlt;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.arr_ready[ab]);
-            ++kc;
-        }
-    } else if (warp >= 4 && warp < 8) {
-        // ===================== Xw and S (lane = token) =====================
-        const int q = warp - 4;
-        const int t = q * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        Walker wk(&p);
-        Chunk c;
-        uint32_t kc = 0;
-        bool ok = true;
-        while (ok && wk.next(c, false)) {
+            return true;
+        };
+
+        if (have_cur) ok = dtprep(c, 0);
+        while (ok && have_cur) {
             const int ab = kc & 1;
             const Arrays &ar = sm.arr[ab];
             const uint32_t tX = 3 * kc + 2;
             const uint8_t *xt = sm.slot[tX % kSlots];
-            // ---- Xw_hi = bf16(w x) into the Xw buffer ----
             if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status) &&
-                       warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status) &&
-                       (kc == 0 || warp_wait(sm, &sm.xbuf_free, 1, status))))
+                       warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status)))
                 break;
-            const float cum_t0 = ar.cum[0][t], cum_t1 = ar.cum[1][t];
-            const float w0 = (t < c.l) ? __expf(ar.cumE[0][3] - cum_t0) * ar.dtp[0][t] : 0.f;
-            const float w1 = (t < c.l) ? __expf(ar.cumE[1][3] - cum_t1) * ar.dtp[1][t] : 0.f;
+            const float w0 = (t < cur_l) ? __expf(ar.E[0] - ar.cum[0][t]) * ar.dtp[0][t] : 0.f;
+            const float w1 = (t < cur_l) ? __expf(ar.E[1] - ar.cum[1][t]) * ar.dtp[1][t] : 0.f;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
+            // ---- dt of the next block while the previous block's state MMAs run ----
+            const bool have_nxt = wk.next(c, false);
+            if (have_nxt && !(ok = dtprep(c, kc + 1))) break;
+            const int32_t nxt_l = c.l;
+            // ---- lo part of Xw into registers ----
+            uint32_t lo[64];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
+                        const uint32_t h2 = pack2(v);
+                        lo[hh * 32 + cc * 4 + e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(h2), -bf16_hi(h2))));
+                    }
+                }
+            }
+            // ---- hi part into the buffer once those MMAs have read it ----
+            if (kc > 0 && !(ok = warp_wait(sm, &sm.xbuf_free, 1, status))) break;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
@@ -600,9 +694,45 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.xhi_ready);
+            // ---- lo part into the buffer once the hi MMA has read it ----
+            if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) =
+                        make_uint4(lo[hh * 32 + cc * 4], lo[hh * 32 + cc * 4 + 1],
+                                   lo[hh * 32 + cc * 4 + 2], lo[hh * 32 + cc * 4 + 3]);
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.xlo_ready);
+            have_cur = have_nxt;
+            cur_l = nxt_l;
+            ++kc;
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ===================== S, row scaling, epilogue (lane = token) =====================
+        const int q = warp - 8;
+        const int t = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        Walker wk(&p);
+        Chunk c;
+        uint32_t kc = 0;
+        bool ok = true;
+        __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.out_y);
+        while (ok && wk.next(c, false)) {
+            const int ab = kc & 1;
+            const Arrays &ar = sm.arr[ab];
+            const uint32_t ycol = kColY + 128 * (kc & 1);
+            const uint8_t *xt = sm.slot[(3 * kc + 2) % kSlots];
             // ---- S_h from G, in place ----
-            if (!(ok = warp_wait(sm, &sm.g_ready, kc & 1, status))) break;
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status) &&
+                       warp_wait(sm, &sm.g_ready, kc & 1, status)))
+                break;
             tc_fence_after();
+            const float cum_t0 = ar.cum[0][t], cum_t1 = ar.cum[1][t];
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t out0[16], out1[16];
@@ -672,55 +802,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             }
             tmem_wait_st();
             tc_fence_before();
+            const float e0 = __expf(cum_t0), e1 = __expf(cum_t1);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.s_ready);
                 mbar_arrive(&sm.arr_free[ab]);
             }
-            // ---- Xw_lo = bf16(w x - Xw_hi) once the hi MMA has read the buffer ----
-            if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
-                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
-                        const uint32_t hi = pack2(v);
-                        o[e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(hi), -bf16_hi(hi))));
-                    }
-                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.xlo_ready);
-            ++kc;
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ===================== epilogue (lane = token) =====================
-        const int q = warp - 8;
-        const int t = q * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        Walker wk(&p);
-        Chunk c;
-        uint32_t kc = 0;
-        bool ok = true;
-        __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.out_y);
-        while (ok && wk.next(c, false)) {
-            const int ab = kc & 1;
-            const uint32_t ycol = kColY + 128 * (kc & 1);
-            const uint8_t *xt = sm.slot[(3 * kc + 2) % kSlots];
             // ---- Y[b] *= exp(cum_t) ----
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
-            const float e0 = __expf(sm.arr[ab].cum[0][t]), e1 = __expf(sm.arr[ab].cum[1][t]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
             if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
             tc_fence_after();
 #pragma unroll
@@ -778,10 +866,12 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (lane == 0) mbar_arrive(&sm.x_epi_done[kc & 1]);
             ++kc;
         }
-    } else {
+    } else if (warp >= 12) {
         // ===================== state (lane = state column n) =====================
-        // Warps 12-13 own n < 64, warps 14-15 n >= 64; C h^T is split the same way
-        // along n, so the bf16 copy of h needs only one half-size buffer.
+        // The accumulator holds hs = h exp(-R).  Per block this role reads hs
+        // (renormalising it when the dt warp asks), writes the bf16 copy of h for
+        // C h^T -- warps 12-13 own n < 64, warps 14-15 n >= 64, matching the two
+        // halves of that MMA -- and stores the final state of each item.
         const int q = warp - 12;
         const int n = q * 32 + lane;
         const bool first_half = q < 2;
@@ -792,16 +882,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         uint32_t kc = 0;
         bool ok = true;
         StT *cache = static_cast<StT *>(p.state_cache);
-        // bf16 copy of 32 state values (head j/2, p block j%2) into this lane's hbuf row
-        auto put_hbuf = [&](int j, const uint32_t (&w)[16]) {
-            uint8_t *rowp = sm.hbuf + (j >> 1) * kHbufHead + hrow * 128;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int chunk = (j & 1) * 4 + cc;
-                *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (hrow & 7)) << 4)) =
-                    make_uint4(w[cc * 4], w[cc * 4 + 1], w[cc * 4 + 2], w[cc * 4 + 3]);
-            }
-        };
+        uint32_t packed[64];                      // bf16 copy of this lane's 128 state values
         while (ok && wk.next(c, true)) {
             const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
             if (c.empty_item) {
@@ -813,30 +894,24 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 }
                 continue;
             }
-            // Entering block kc: the state source is the cache slot (first block of the
-            // item) or the TMEM accumulator after block kc-1.  Each lane writes its bf16
-            // copy into hbuf once C h^T may overwrite it (first half of n after the
-            // previous block's C h^T, second half after this block's first-half C h^T),
-            // and stores state * exp(cum_end of block kc) back into TMEM.
-            const bool from_cache = c.first;
-            if (!from_cache) {
-                // wait for this block's predecessor to finish its state MMAs
+            const int ab = kc & 1;
+            const Arrays &ar = sm.arr[ab];
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
+            if (!c.first) {
                 if (!(ok = warp_wait(sm, &sm.state_done, (kc - 1) & 1, status))) break;
                 tc_fence_after();
             }
-            const int ab = kc & 1;
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
-            const float2 dd0 = make_float2(__expf(sm.arr[ab].cumE[0][3]), __expf(sm.arr[ab].cumE[0][3]));
-            const float2 dd1 = make_float2(__expf(sm.arr[ab].cumE[1][3]), __expf(sm.arr[ab].cumE[1][3]));
-            if (first_half) {
-                if (kc > 0 && !(ok = warp_wait(sm, &sm.yinter_ready, (kc - 1) & 1, status))) break;
-            } else {
-                if (!(ok = warp_wait(sm, &sm.hbuf_a_done, kc & 1, status))) break;
-            }
+            // per head: the state entering the block is hs * eprev; renormalised
+            // accumulators hold exp(dlt) h instead
+            const float2 ep0 = make_float2(ar.eprev[0], ar.eprev[0]), ep1 = make_float2(ar.eprev[1], ar.eprev[1]);
+            const float2 ed0 = make_float2(ar.edlt[0], ar.edlt[0]), ed1 = make_float2(ar.edlt[1], ar.edlt[1]);
+            const bool rn0 = ar.renorm[0] != 0, rn1 = ar.renorm[1] != 0;
+            const bool write_tmem = c.first || rn0 || rn1;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                const int hh = j >> 1;
                 uint32_t r[32];
-                if (from_cache) {
+                if (c.first) {
 #pragma unroll
                     for (int i2 = 0; i2 < 32; ++i2)
                         r[i2] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 32 + i2) * kN) : 0.f);
@@ -844,29 +919,47 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                     tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
                     tmem_wait_ld();
                 }
-                uint32_t w[16];
+                const float2 ep = hh ? ep1 : ep0, ed = hh ? ed1 : ed0;
+                const bool rn = hh ? rn1 : rn0;
 #pragma unroll
                 for (int i2 = 0; i2 < 16; ++i2) {
-                    const float2 v = f2(r[2 * i2], r[2 * i2 + 1]);
-                    w[i2] = pack2(v);
-                    const float2 sv = __fmul2_rn(v, (j >> 1) ? dd1 : dd0);
-                    r[2 * i2] = __float_as_uint(sv.x);
-                    r[2 * i2 + 1] = __float_as_uint(sv.y);
+                    // h entering the block (the cache values are h itself, eprev = 1 there)
+                    const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep);
+                    packed[j * 16 + i2] = pack2(h);
+                    const float2 acc = rn ? __fmul2_rn(h, ed) : f2(r[2 * i2], r[2 * i2 + 1]);
+                    r[2 * i2] = __float_as_uint(acc.x);
+                    r[2 * i2 + 1] = __float_as_uint(acc.y);
                 }
-                put_hbuf(j, w);
-                tmem_st32(tmem + lane_off + kColH + 32 * j, r);
+                if (write_tmem) tmem_st32(tmem + lane_off + kColH + 32 * j, r);
             }
-            fence_proxy_async_smem();
-            tmem_wait_st();
+            if (write_tmem) tmem_wait_st();
+            const float2 ef0 = make_float2(ar.eend[0], ar.eend[0]), ef1 = make_float2(ar.eend[1], ar.eend[1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(first_half ? &sm.hs_a : &sm.hs_b);
-                mbar_arrive(&sm.state_ready);
+                mbar_arrive(&sm.state_ok);
                 mbar_arrive(&sm.arr_free[ab]);
             }
+            // ---- bf16 copy of h for C h^T ----
+            if (first_half) {
+                if (kc > 0 && !(ok = warp_wait(sm, &sm.yinter_ready, (kc - 1) & 1, status))) break;
+            } else {
+                if (!(ok = warp_wait(sm, &sm.hbuf_a_done, kc & 1, status))) break;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint8_t *rowp = sm.hbuf + hh * kHbufHead + hrow * 128;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(rowp + ((cc ^ (hrow & 7)) << 4)) =
+                        make_uint4(packed[hh * 32 + cc * 4], packed[hh * 32 + cc * 4 + 1],
+                                   packed[hh * 32 + cc * 4 + 2], packed[hh * 32 + cc * 4 + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(first_half ? &sm.hs_a : &sm.hs_b);
             if (c.last) {
-                // final state of the item, straight from the accumulator
+                // final state of the item: h = hs * exp(R after the block)
                 if (!(ok = warp_wait(sm, &sm.state_done, kc & 1, status))) break;
                 tc_fence_after();
                 if (p.write_final) {
@@ -875,9 +968,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                         uint32_t r[32];
                         tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
                         tmem_wait_ld();
+                        const float2 ef = (j >> 1) ? ef1 : ef0;
 #pragma unroll
-                        for (int i2 = 0; i2 < 32; ++i2)
-                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + i2) * kN, __uint_as_float(r[i2]));
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ef);
+                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + 2 * i2) * kN, h.x);
+                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + 2 * i2 + 1) * kN, h.y);
+                        }
                     }
                 }
                 tc_fence_before();

@@ -200,3 +200,20 @@ def test_many_short_sequences_and_empty_ones():
     p = W.make_problem(lens, nheads=8, headdim=64, dstate=128, ngroups=2, num_slots=80,
                        has_init=(rng.random(60) < 0.5).astype(np.uint8), cache_std=0.3, seed=47)
     _run_and_check(p)
+
+
+@pytest.mark.parametrize("regime", ["steep", "flat"])
+def test_decay_regimes(regime):
+    """Steep decay (32-token blocks decaying by more than e^80: per-element exp path and a
+    renormalised state every block) and near-zero decay (the running scale never renormalises)."""
+    p = W.make_problem([700, 129, 40], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
+                       has_init=[1, 0, 1], cache_std=0.1, dt_softplus=False, with_dt_bias=False,
+                       state_dtype="f32", seed=48)
+    rng = np.random.default_rng(49)
+    if regime == "steep":
+        p.dt = rng.uniform(0.3, 0.6, size=p.dt.shape).astype(np.float32)
+        p.A = np.array([-16.0, -12.0, -9.0, -3.0], dtype=np.float32)
+    else:
+        p.dt = rng.uniform(0.001, 0.1, size=p.dt.shape).astype(np.float32)
+        p.A = np.array([-1e-3, -1e-4, -2e-3, 0.0], dtype=np.float32)
+    _run_and_check(p)
