@@ -62,6 +62,7 @@ constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kHbufHead = 8192;    // one head of the half-n bf16 state copy: 64 rows x 128 B
 constexpr int kThreads = 512;     // 16 warps, each with exactly one role below
+
 constexpr uint64_t kSpinLimit = 4000000000ull;   // clock cycles (~2 s) per wait
 constexpr float kDiagFactorLimit = 80.f;         // |decay| of a 32-token block for the
                                                  // factored diagonal path (e^80 < fp32 max)
@@ -143,77 +144,91 @@ static_assert(offsetof(Smem, xw) % 1024 == 0 && offsetof(Smem, hbuf) % 1024 == 0
 // ---------------------------------------------------------------------------
 struct Chunk {
     int32_t seq, h0, g, slot;
-    int64_t row0;        // first token of this block
+    int32_t row0;        // first token of this block (total tokens < 2^31 on this path)
     int32_t l;           // valid tokens in this block
     bool init, first, last, empty_item;
 };
 
-struct Walker {
-    const Params *p;
-    int cta, grid;
-    int round = 0;
-    bool have = false;
-    int32_t seq = 0, h0 = 0, g = 0, slot = 0, len = 0, nb = 0, b = 0;
-    int64_t t0 = 0;
-    bool init = false;
+// One work item: a sequence and a pair of heads of one B/C group.
+struct Item {
+    int32_t round;                // deal round after this item
+    int32_t seq, h0, g, slot, t0, len;
+    int32_t flags;                // bit 0: found, bit 1: has an initial state
+};
 
-    __device__ Walker(const Params *pp) : p(pp), cta(blockIdx.x), grid(gridDim.x) {}
-
-    // Next valid item (longest sequences first, snake order over the CTAs).
-    __device__ bool next_item(bool report) {
-        const int hp_per_seq = p->H / 2;
-        while (true) {
-            const int64_t base = (int64_t)round * grid;
-            const int64_t idx = base + ((round & 1) ? (grid - 1 - cta) : cta);
-            ++round;
-            if (base >= p->num_items) return false;
-            if (idx >= p->num_items) continue;
-            const int rank = (int)(idx / hp_per_seq);
-            const int hp = (int)(idx % hp_per_seq);
-            seq = p->order[rank];
-            h0 = hp * 2;
-            g = h0 / p->hpg;
-            const int64_t a = p->cu_seqlens[seq], e = p->cu_seqlens[seq + 1];
-            if (a < 0 || e < a || e > p->T) {
-                if (report && p->device_status) atomicOr(p->device_status, SSD_DEV_BAD_SEQLENS);
+// Next valid item of this CTA (longest sequences first, snake order over the
+// CTAs), starting at deal round `round`.  Out of line: called once per item.
+__device__ __noinline__ Item find_item(const Params &p, int32_t round, bool report) {
+    Item it;
+    it.flags = 0;
+    const int32_t hp_per_seq = p.H / 2;
+    const int32_t grid = gridDim.x, cta = blockIdx.x;
+    while (true) {
+        const int32_t base = round * grid;
+        const int32_t idx = base + ((round & 1) ? (grid - 1 - cta) : cta);
+        ++round;
+        if (base >= p.num_items) break;
+        if (idx >= p.num_items) continue;
+        const int32_t rank = idx / hp_per_seq;
+        const int32_t hp = idx - rank * hp_per_seq;
+        const int32_t seq = p.order[rank];
+        const int32_t h0 = hp * 2;
+        const int64_t a = p.cu_seqlens[seq], e = p.cu_seqlens[seq + 1];
+        if (a < 0 || e < a || e > p.T) {
+            if (report && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SEQLENS);
+            continue;
+        }
+        const bool init = p.has_init != nullptr && p.has_init[seq] != 0;
+        int32_t slot = 0;
+        if (init || p.write_final) {
+            slot = p.slot_idx[seq];
+            if (slot < 0 || slot >= p.num_slots) {
+                if (report && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SLOT);
                 continue;
             }
-            init = p->has_init != nullptr && p->has_init[seq] != 0;
-            slot = 0;
-            if (init || p->write_final) {
-                slot = p->slot_idx[seq];
-                if (slot < 0 || slot >= p->num_slots) {
-                    if (report && p->device_status) atomicOr(p->device_status, SSD_DEV_BAD_SLOT);
-                    continue;
-                }
-            }
-            t0 = a;
-            len = (int32_t)(e - a);
-            nb = (len + kQ - 1) / kQ;
-            b = 0;
-            return true;
         }
+        it.seq = seq;
+        it.h0 = h0;
+        it.g = h0 / p.hpg;
+        it.slot = slot;
+        it.t0 = (int32_t)a;
+        it.len = (int32_t)(e - a);
+        it.flags = 1 | (init ? 2 : 0);
+        break;
     }
+    it.round = round;
+    return it;
+}
+
+// Walks this CTA's items block by block; identical in every role.
+struct Walker {
+    Item it;
+    int32_t nb = 0, b = 0;
+    bool have = false;
+
+    __device__ Walker() { it.round = 0; }
 
     // Next event: a block of an item, or (if want_empty) an item without tokens.
-    __device__ bool next(Chunk &c, bool want_empty, bool report = false) {
+    __device__ bool next(const Params &p, Chunk &c, bool want_empty, bool report = false) {
         while (true) {
             if (!have || b >= nb) {
-                if (!next_item(report)) return false;
+                it = find_item(p, it.round, report);
+                if (!(it.flags & 1)) return false;
                 have = true;
+                nb = (it.len + kQ - 1) / kQ;
+                b = 0;
                 if (nb == 0) {
-                    b = 0;
                     if (want_empty) {
-                        c.seq = seq; c.h0 = h0; c.g = g; c.slot = slot; c.row0 = t0; c.l = 0;
-                        c.init = init; c.first = c.last = true; c.empty_item = true;
+                        c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot; c.row0 = it.t0; c.l = 0;
+                        c.init = (it.flags & 2) != 0; c.first = c.last = true; c.empty_item = true;
                         return true;
                     }
                     continue;
                 }
             }
-            c.seq = seq; c.h0 = h0; c.g = g; c.slot = slot; c.init = init;
-            c.row0 = t0 + (int64_t)b * kQ;
-            c.l = min(kQ, len - b * kQ);
+            c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot; c.init = (it.flags & 2) != 0;
+            c.row0 = it.t0 + b * kQ;
+            c.l = min(kQ, it.len - b * kQ);
             c.first = (b == 0);
             c.last = (b == nb - 1);
             c.empty_item = false;
@@ -226,10 +241,10 @@ struct Walker {
 // ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
-// Single-thread wait (producer / MMA issuer).
-__device__ __forceinline__ bool wait_bar(Smem &sm, uint64_t *bar, uint32_t parity,
-                                         int32_t *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waits test the barrier once inline; the bounded spin is out of line so
+// that the many call sites stay small (the whole kernel's hot code has to fit
+// the SM's instruction cache).
+__device__ __noinline__ bool wait_bar_slow(Smem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
     const uint64_t t_start = clock64();
     uint32_t it = 0;
     while (!mbar_try_wait(bar, parity)) {
@@ -245,12 +260,12 @@ __device__ __forceinline__ bool wait_bar(Smem &sm, uint64_t *bar, uint32_t parit
     return true;
 }
 
-// Whole-warp wait with a warp-uniform result (all 32 lanes must call it).
-// A barrier phase never runs two completions ahead of its slowest waiter in
-// this kernel, so once one lane observes completion every lane will.
-__device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t parity,
-                                          int32_t *status) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+// Single-thread wait (producer / MMA issuer).
+__device__ __forceinline__ bool wait_bar(Smem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
+    return mbar_try_wait(bar, parity) || wait_bar_slow(sm, bar, parity, status);
+}
+
+__device__ __noinline__ bool warp_wait_slow(Smem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
     const uint64_t t_start = clock64();
     uint32_t it = 0;
     while (true) {
@@ -269,6 +284,13 @@ __device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t pari
             if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
         }
     }
+}
+
+// Whole-warp wait with a warp-uniform result (all 32 lanes must call it).
+// A barrier phase never runs two completions ahead of its slowest waiter in
+// this kernel, so once one lane observes completion every lane will.
+__device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
+    return __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) || warp_wait_slow(sm, bar, parity, status);
 }
 
 __device__ __forceinline__ float softplus_f(float z) {
@@ -337,6 +359,139 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16(v.x, v.y); }
 
+// S on a diagonal 32-token block whose decay is too steep for the factored
+// form: exp(cum_t - cum_s) dt'_s per element, G read from and S written back to
+// the 32 TMEM columns at taddr.  Rare; out of line.
+__device__ __noinline__ void s_diag_exact(uint32_t taddr, const Arrays &ar, int t, int j, float cum_t0,
+                                          float cum_t1) {
+    uint32_t g[32], out0[16], out1[16];
+    tmem_ld32(taddr, g);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i2 = 0; i2 < 16; ++i2) {
+        const int s = 32 * j + 2 * i2;
+        float r0[2], r1[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float gv = __uint_as_float(g[2 * i2 + e]);
+            const bool keep = (s + e) <= t;
+            r0[e] = keep ? gv * (__expf(cum_t0 - ar.cum[0][s + e]) * ar.dtp[0][s + e]) : 0.f;
+            r1[e] = keep ? gv * (__expf(cum_t1 - ar.cum[1][s + e]) * ar.dtp[1][s + e]) : 0.f;
+        }
+        out0[i2] = pack_bf16(r0[0], r0[1]);
+        out1[i2] = pack_bf16(r1[0], r1[1]);
+    }
+    tmem_st16(taddr, out0);
+    tmem_st16(taddr + 16, out1);
+}
+
+// dt softplus, the within-block cumsum of dt' A and the per-block scales of one
+// block, computed by the four token warps (lane = token) into sm.arr[k & 1].
+// R0/R1 carry the running scale of the state accumulator per head (0 at the
+// first block of an item).  Out of line: one call site, shared code.
+struct DtOut {
+    float R0, R1;
+    int32_t ok;
+};
+__device__ __noinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0, int32_t l, int32_t h0,
+                                      bool first, uint32_t k, float R0, float R1, int32_t *status) {
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) - 4;
+    const int t = q * 32 + lane;
+    DtOut out;
+    out.R0 = first ? 0.f : R0;
+    out.R1 = first ? 0.f : R1;
+    out.ok = 0;
+    const int ab = k & 1;
+    Arrays &ar = sm.arr[ab];
+    if (k >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((k >> 1) - 1) & 1, status)) return out;
+    float d0 = 0.f, d1 = 0.f;
+    if (t < l) {
+        const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + t) * p.H + h0);
+        const float z0 = raw.x + (p.dt_bias ? p.dt_bias[h0] : 0.f);
+        const float z1 = raw.y + (p.dt_bias ? p.dt_bias[h0 + 1] : 0.f);
+        d0 = p.dt_softplus ? softplus_f(z0) : z0;
+        d1 = p.dt_softplus ? softplus_f(z1) : z1;
+    }
+    float s0 = d0 * p.A[h0], s1 = d1 * p.A[h0 + 1];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float v0 = __shfl_up_sync(0xffffffffu, s0, off);
+        const float v1 = __shfl_up_sync(0xffffffffu, s1, off);
+        if (lane >= off) { s0 += v0; s1 += v1; }
+    }
+    // warp extremes of the local scan (the block's cum range follows from them)
+    float mn0 = s0, mx0 = s0, mn1 = s1, mx1 = s1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, off));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    if (lane == 31) {
+        ar.wtot[0][q] = s0; ar.wtot[1][q] = s1;
+        ar.wmin[0][q] = mn0; ar.wmin[1][q] = mn1;
+        ar.wmax[0][q] = mx0; ar.wmax[1][q] = mx1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.scan_bar[ab]);
+    if (!warp_wait(sm, &sm.scan_bar[ab], (k >> 1) & 1, status)) return out;
+    float cE[2][4], lo[2], hi[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float run = 0.f;
+        lo[hh] = 0.f;
+        hi[hh] = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            lo[hh] = fminf(lo[hh], run + ar.wmin[hh][w]);
+            hi[hh] = fmaxf(hi[hh], run + ar.wmax[hh][w]);
+            run += ar.wtot[hh][w];
+            cE[hh][w] = run;
+        }
+    }
+    // cum before and at the end of this warp's 32-token block (static indices only)
+    float pre0 = 0.f, pre1 = 0.f, end0 = cE[0][0], end1 = cE[1][0];
+#pragma unroll
+    for (int w = 1; w < 4; ++w)
+        if (q == w) { pre0 = cE[0][w - 1]; pre1 = cE[1][w - 1]; end0 = cE[0][w]; end1 = cE[1][w]; }
+    const float c0 = s0 + pre0, c1 = s1 + pre1;
+    ar.cum[0][t] = c0;
+    ar.cum[1][t] = c1;
+    ar.dtp[0][t] = d0;
+    ar.dtp[1][t] = d1;
+    ar.vfac[0][t] = d0 != 0.f ? __expf(end0 - c0) * d0 : 0.f;
+    ar.vfac[1][t] = d1 != 0.f ? __expf(end1 - c1) * d1 : 0.f;
+    ar.vdiag[0][t] = d0 != 0.f ? __expf(fminf(pre0 - c0, kDiagFactorLimit)) * d0 : 0.f;
+    ar.vdiag[1][t] = d1 != 0.f ? __expf(fminf(pre1 - c1, kDiagFactorLimit)) * d1 : 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float &R = hh ? out.R1 : out.R0;
+        const float dlt = cE[hh][3];
+        const bool fast = (-R - lo[hh] <= kScaleLimit) && (-R - hi[hh] >= -kScaleLimit);
+        const float Rp = fast ? R : -dlt;          // scale in force for this block
+        if (t == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ar.cumE[hh][j] = cE[hh][j];
+                const float cb = j ? cE[hh][j - 1] : 0.f;
+                ar.exact[hh][j] = fabsf(cE[hh][j] - cb) > kDiagFactorLimit;
+            }
+            ar.E[hh] = -Rp;
+            ar.eprev[hh] = __expf(R);
+            ar.edlt[hh] = __expf(dlt);
+            ar.eend[hh] = __expf(Rp + dlt);
+            ar.renorm[hh] = fast ? 0 : 1;
+        }
+        R = Rp + dlt;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.arr_ready[ab]);
+    out.ok = 1;
+    return out;
+}
+
 template <typename StT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
@@ -383,18 +538,19 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
     const uint32_t tmem = sm.tmem_base;
     int32_t *status = p.device_status;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      if (warp == 0) {
         // ===================== TMA producer =====================
         if (lane == 0) {
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_b);
             tma_prefetch_desc(&map_c);
-            Walker wk(&p);
+            Walker wk;
             Chunk c;
             uint32_t kc = 0, issued = 0;
             bool ok = true;
-            while (ok && wk.next(c, false, true)) {
-                const int32_t row = (int32_t)c.row0;
+            while (ok && wk.next(p, c, false, true)) {
+                const int32_t row = c.row0;
                 for (int j = 0; j < 3; ++j) {                    // C, B, X
                     const uint32_t tile = 3 * kc + j, slot = tile % kSlots, use = tile / kSlots;
                     const CUtensorMap *m = (j == 0) ? &map_c : (j == 1) ? &map_b : &map_x;
@@ -425,12 +581,12 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
     } else if (warp == 1) {
         // ===================== MMA issuer, output path =====================
         if (lane == 0) {
-            Walker wk(&p);
+            Walker wk;
             Chunk c;
             uint32_t kc = 0;
             bool ok = true;
             const uint32_t bH = smem_u32(sm.hbuf);
-            while (ok && wk.next(c, false)) {
+            while (ok && wk.next(p, c, false)) {
                 const uint32_t tC = 3 * kc, tB = 3 * kc + 1, tX = 3 * kc + 2;
                 const uint32_t bC = smem_u32(sm.slot[tC % kSlots]);
                 const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
@@ -494,12 +650,12 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
     } else if (warp == 3) {
         // ===================== MMA issuer, state path =====================
         if (lane == 0) {
-            Walker wk(&p);
+            Walker wk;
             Chunk c;
             uint32_t kc = 0;
             bool ok = true;
             const uint32_t bW = smem_u32(sm.xw[0]);
-            while (ok && wk.next(c, false)) {
+            while (ok && wk.next(p, c, false)) {
                 const uint32_t tB = 3 * kc + 1, tX = 3 * kc + 2;
                 const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
                 // ---- hs += B^T Xw_hi ----
@@ -529,117 +685,28 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             mma_commit(&sm.drain_h);
             wait_bar(sm, &sm.drain_h, 0, nullptr);
         }
-    } else if (warp == 2) {
-        // TMEM owner only: allocates above, frees after the final barrier
+      }
+      // warp 2: TMEM owner only (allocates above, frees after the final barrier)
     } else if (warp >= 4 && warp < 8) {
         // ===================== dt, scales and the scaled Xw (lane = token) =====================
-        // Per block k (once X lands): the dt arrays of block k+1, the lo part of
-        // Xw into registers, the hi part into the Xw buffer once block k-1's
-        // state MMAs have read it, the lo part once the hi MMA has read it.  Only
-        // the two buffer fills sit on the state recurrence's critical path.
+        // Per block k (once X lands): the dt arrays of block k+1, then the hi
+        // part of Xw into the Xw buffer once block k-1's state MMAs have read it,
+        // then the lo part once the hi MMA has read it.
         const int q = warp - 4;
         const int t = q * 32 + lane;
-        Walker wk(&p);
+        Walker wk;
         Chunk c;
-        bool have_cur = wk.next(c, false);
+        bool have_cur = wk.next(p, c, false);
         int32_t cur_l = c.l;                      // valid tokens of the block being filled
         uint32_t kc = 0;
         bool ok = true;
-        float R0 = 0.f, R1 = 0.f;                 // running scale of the state accumulator
-
-        // dt softplus, within-block cumsum and the per-block scales of block k
-        auto dtprep = [&](const Chunk &c, uint32_t k) -> bool {
-            const int ab = k & 1;
-            Arrays &ar = sm.arr[ab];
-            if (k >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((k >> 1) - 1) & 1, status)) return false;
-            if (c.first) { R0 = 0.f; R1 = 0.f; }
-            float d0 = 0.f, d1 = 0.f;
-            if (t < c.l) {
-                const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (c.row0 + t) * p.H + c.h0);
-                const float z0 = raw.x + (p.dt_bias ? p.dt_bias[c.h0] : 0.f);
-                const float z1 = raw.y + (p.dt_bias ? p.dt_bias[c.h0 + 1] : 0.f);
-                d0 = p.dt_softplus ? softplus_f(z0) : z0;
-                d1 = p.dt_softplus ? softplus_f(z1) : z1;
-            }
-            float s0 = d0 * p.A[c.h0], s1 = d1 * p.A[c.h0 + 1];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float v0 = __shfl_up_sync(0xffffffffu, s0, off);
-                const float v1 = __shfl_up_sync(0xffffffffu, s1, off);
-                if (lane >= off) { s0 += v0; s1 += v1; }
-            }
-            // warp extremes of the local scan (the block's cum range follows from them)
-            float mn0 = s0, mx0 = s0, mn1 = s1, mx1 = s1;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, off));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            if (lane == 31) {
-                ar.wtot[0][q] = s0; ar.wtot[1][q] = s1;
-                ar.wmin[0][q] = mn0; ar.wmin[1][q] = mn1;
-                ar.wmax[0][q] = mx0; ar.wmax[1][q] = mx1;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.scan_bar[ab]);
-            if (!warp_wait(sm, &sm.scan_bar[ab], (k >> 1) & 1, status)) return false;
-            float cE[2][4], lo[2], hi[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float run = 0.f;
-                lo[hh] = 0.f;
-                hi[hh] = 0.f;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    lo[hh] = fminf(lo[hh], run + ar.wmin[hh][w]);
-                    hi[hh] = fmaxf(hi[hh], run + ar.wmax[hh][w]);
-                    run += ar.wtot[hh][w];
-                    cE[hh][w] = run;
-                }
-            }
-            // cum before and at the end of this warp's 32-token block (static indices only)
-            float pre0 = 0.f, pre1 = 0.f, end0 = cE[0][0], end1 = cE[1][0];
-#pragma unroll
-            for (int w = 1; w < 4; ++w)
-                if (q == w) { pre0 = cE[0][w - 1]; pre1 = cE[1][w - 1]; end0 = cE[0][w]; end1 = cE[1][w]; }
-            const float c0 = s0 + pre0, c1 = s1 + pre1;
-            ar.cum[0][t] = c0;
-            ar.cum[1][t] = c1;
-            ar.dtp[0][t] = d0;
-            ar.dtp[1][t] = d1;
-            ar.vfac[0][t] = d0 != 0.f ? __expf(end0 - c0) * d0 : 0.f;
-            ar.vfac[1][t] = d1 != 0.f ? __expf(end1 - c1) * d1 : 0.f;
-            ar.vdiag[0][t] = d0 != 0.f ? __expf(fminf(pre0 - c0, kDiagFactorLimit)) * d0 : 0.f;
-            ar.vdiag[1][t] = d1 != 0.f ? __expf(fminf(pre1 - c1, kDiagFactorLimit)) * d1 : 0.f;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float &R = hh ? R1 : R0;
-                const float dlt = cE[hh][3];
-                const bool fast = (-R - lo[hh] <= kScaleLimit) && (-R - hi[hh] >= -kScaleLimit);
-                const float Rp = fast ? R : -dlt;          // scale in force for this block
-                if (t == 0) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        ar.cumE[hh][j] = cE[hh][j];
-                        const float cb = j ? cE[hh][j - 1] : 0.f;
-                        ar.exact[hh][j] = fabsf(cE[hh][j] - cb) > kDiagFactorLimit;
-                    }
-                    ar.E[hh] = -Rp;
-                    ar.eprev[hh] = __expf(R);
-                    ar.edlt[hh] = __expf(dlt);
-                    ar.eend[hh] = __expf(Rp + dlt);
-                    ar.renorm[hh] = fast ? 0 : 1;
-                }
-                R = Rp + dlt;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.arr_ready[ab]);
-            return true;
-        };
-
-        if (have_cur) ok = dtprep(c, 0);
+        DtOut ds;                                 // running scale of the state accumulator
+        ds.R0 = ds.R1 = 0.f;
+        ds.ok = 1;
+        if (have_cur) {
+            ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, 0, ds.R0, ds.R1, status);
+            ok = ds.ok != 0;
+        }
         while (ok && have_cur) {
             const int ab = kc & 1;
             const Arrays &ar = sm.arr[ab];
@@ -653,33 +720,18 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
             // ---- dt of the next block while the previous block's state MMAs run ----
-            const bool have_nxt = wk.next(c, false);
-            if (have_nxt && !(ok = dtprep(c, kc + 1))) break;
-            const int32_t nxt_l = c.l;
-            // ---- lo part of Xw into registers ----
-            uint32_t lo[64];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
-                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
-                        const uint32_t h2 = pack2(v);
-                        lo[hh * 32 + cc * 4 + e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(h2), -bf16_hi(h2))));
-                    }
-                }
+            const bool have_nxt = wk.next(p, c, false);
+            if (have_nxt) {
+                ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, kc + 1, ds.R0, ds.R1, status);
+                if (!(ok = ds.ok != 0)) break;
             }
+            const int32_t nxt_l = c.l;
             // ---- hi part into the buffer once those MMAs have read it ----
             if (kc > 0 && !(ok = warp_wait(sm, &sm.xbuf_free, 1, status))) break;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
-#pragma unroll
+#pragma unroll 2
                 for (int cc = 0; cc < 8; ++cc) {
                     const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
                     const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
@@ -694,17 +746,26 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.xhi_ready);
-            // ---- lo part into the buffer once the hi MMA has read it ----
+            // ---- lo part = bf16(w x - hi) into the buffer once the hi MMA has read it ----
             if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
+#pragma unroll 2
                 for (int cc = 0; cc < 8; ++cc) {
                     const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) =
-                        make_uint4(lo[hh * 32 + cc * 4], lo[hh * 32 + cc * 4 + 1],
-                                   lo[hh * 32 + cc * 4 + 2], lo[hh * 32 + cc * 4 + 3]);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
+                        const uint32_t h2 = pack2(v);
+                        o[e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(h2), -bf16_hi(h2))));
+                    }
+                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.xlo_ready);
@@ -717,12 +778,12 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         const int q = warp - 8;
         const int t = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        Walker wk(&p);
+        Walker wk;
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
         __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.out_y);
-        while (ok && wk.next(c, false)) {
+        while (ok && wk.next(p, c, false)) {
             const int ab = kc & 1;
             const Arrays &ar = sm.arr[ab];
             const uint32_t ycol = kColY + 128 * (kc & 1);
@@ -735,70 +796,45 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             const float cum_t0 = ar.cum[0][t], cum_t1 = ar.cum[1][t];
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
-                uint32_t out0[16], out1[16];
-                if (j > q) {
-#pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2) { out0[i2] = 0u; out1[i2] = 0u; }
-                } else {
-                    uint32_t g[32];
-                    tmem_ld32(tmem + lane_off + kColG + 32 * j, g);
-                    if (j < q) {
-                        // both factors <= 1: exp(cum_t - cum_e) exp(cum_e - cum_s), cum_e = end of block j
-                        const float u0 = __expf(cum_t0 - ar.cumE[0][j]);
-                        const float u1 = __expf(cum_t1 - ar.cumE[1][j]);
-                        const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) {
-                            const int s = 32 * j + 2 * i2;
-                            const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
-                            const float2 v0 = *reinterpret_cast<const float2 *>(&ar.vfac[0][s]);
-                            const float2 v1 = *reinterpret_cast<const float2 *>(&ar.vfac[1][s]);
-                            out0[i2] = pack2(__fmul2_rn(__fmul2_rn(gg, uu0), v0));
-                            out1[i2] = pack2(__fmul2_rn(__fmul2_rn(gg, uu1), v1));
-                        }
-                    } else if (!ar.exact[0][j] && !ar.exact[1][j]) {
-                        // diagonal block, factored at the block start: exp(cum_t - cum_b) <= 1,
-                        // exp(cum_b - cum_s) <= exp(kDiagFactorLimit)
-                        const float cb0 = j ? ar.cumE[0][j - 1] : 0.f;
-                        const float cb1 = j ? ar.cumE[1][j - 1] : 0.f;
-                        const float u0 = __expf(cum_t0 - cb0), u1 = __expf(cum_t1 - cb1);
-                        const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) {
-                            const int s = 32 * j + 2 * i2;
-                            const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
-                            const float2 v0 = *reinterpret_cast<const float2 *>(&ar.vdiag[0][s]);
-                            const float2 v1 = *reinterpret_cast<const float2 *>(&ar.vdiag[1][s]);
-                            float2 r0 = __fmul2_rn(__fmul2_rn(gg, uu0), v0);
-                            float2 r1 = __fmul2_rn(__fmul2_rn(gg, uu1), v1);
-                            if (s > t) { r0.x = 0.f; r1.x = 0.f; }
-                            if (s + 1 > t) { r0.y = 0.f; r1.y = 0.f; }
-                            out0[i2] = pack2(r0);
-                            out1[i2] = pack2(r1);
-                        }
-                    } else {
-                        // diagonal block with a steep decay: one exp per element
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) {
-                            const int s = 32 * j + 2 * i2;
-                            float r0[2], r1[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const float gv = __uint_as_float(g[2 * i2 + e]);
-                                const bool keep = (s + e) <= t;
-                                r0[e] = keep ? gv * (__expf(cum_t0 - ar.cum[0][s + e]) * ar.dtp[0][s + e]) : 0.f;
-                                r1[e] = keep ? gv * (__expf(cum_t1 - ar.cum[1][s + e]) * ar.dtp[1][s + e]) : 0.f;
-                            }
-                            out0[i2] = pack_bf16(r0[0], r0[1]);
-                            out1[i2] = pack_bf16(r1[0], r1[1]);
-                        }
-                    }
+                const uint32_t taddr = tmem + lane_off + kColG + 32 * j;
+                if (j == q && (ar.exact[0][j] || ar.exact[1][j])) {
+                    s_diag_exact(taddr, ar, t, j, cum_t0, cum_t1);   // steep decay: rare
+                    continue;
                 }
-                tmem_st16(tmem + lane_off + kColG + 32 * j, out0);
-                tmem_st16(tmem + lane_off + kColG + 32 * j + 16, out1);
+                // exp(cum_t - cum_s) = exp(cum_t - c_b) exp(c_b - cum_s): below the
+                // diagonal c_b is the end of block j (both factors <= 1), on it the
+                // start of the block (first factor <= 1, second <= exp(kDiagFactorLimit));
+                // the second factor times dt'_s is precomputed per token.  One code
+                // path for every j: tokens s at or beyond `lim` (causal mask, or the
+                // whole block above the diagonal) are selected to 0.
+                uint32_t g[32], out0[16], out1[16];
+                tmem_ld32(taddr, g);
+                const bool diag = (j == q);
+                const int lim = j < q ? 32 : (diag ? t - 32 * j + 1 : 0);
+                const float b0 = diag ? (j ? ar.cumE[0][j - 1] : 0.f) : ar.cumE[0][j];
+                const float b1 = diag ? (j ? ar.cumE[1][j - 1] : 0.f) : ar.cumE[1][j];
+                const float *v0p = (diag ? ar.vdiag[0] : ar.vfac[0]) + 32 * j;
+                const float *v1p = (diag ? ar.vdiag[1] : ar.vfac[1]) + 32 * j;
+                const float u0 = __expf(cum_t0 - b0), u1 = __expf(cum_t1 - b1);
+                const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
+                    const float2 v0 = *reinterpret_cast<const float2 *>(v0p + 2 * i2);
+                    const float2 v1 = *reinterpret_cast<const float2 *>(v1p + 2 * i2);
+                    float2 r0 = __fmul2_rn(__fmul2_rn(gg, uu0), v0);
+                    float2 r1 = __fmul2_rn(__fmul2_rn(gg, uu1), v1);
+                    const bool kx = 2 * i2 < lim, ky = 2 * i2 + 1 < lim;
+                    r0.x = kx ? r0.x : 0.f;
+                    r1.x = kx ? r1.x : 0.f;
+                    r0.y = ky ? r0.y : 0.f;
+                    r1.y = ky ? r1.y : 0.f;
+                    out0[i2] = pack2(r0);
+                    out1[i2] = pack2(r1);
+                }
+                tmem_st16(taddr, out0);
+                tmem_st16(taddr + 16, out1);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -811,7 +847,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             // ---- Y[b] *= exp(cum_t) ----
             if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
@@ -831,11 +867,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (lane == 0) mbar_arrive(&sm.y_scaled);
             // ---- y = Y + D x (x from the smem tile, which stays until x_epi_done) ----
             const bool valid = t < c.l;
-            const int64_t grow = (c.row0 + t) * (int64_t)p.H * kP + (int64_t)c.h0 * kP;
+            const int64_t grow = (int64_t)(c.row0 + t) * p.H * kP + (int64_t)c.h0 * kP;
             const float D0 = p.D ? p.D[c.h0] : 0.f, D1 = p.D ? p.D[c.h0 + 1] : 0.f;
             if (!(ok = warp_wait(sm, &sm.y_ready, kc & 1, status))) break;
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
@@ -877,13 +913,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         const bool first_half = q < 2;
         const int hrow = n & 63;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        Walker wk(&p);
+        Walker wk;
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
         StT *cache = static_cast<StT *>(p.state_cache);
         uint32_t packed[64];                      // bf16 copy of this lane's 128 state values
-        while (ok && wk.next(c, true)) {
+        while (ok && wk.next(p, c, true)) {
             const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
             if (c.empty_item) {
                 if (p.write_final) {
@@ -908,29 +944,29 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             const bool rn0 = ar.renorm[0] != 0, rn1 = ar.renorm[1] != 0;
             const bool write_tmem = c.first || rn0 || rn1;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int hh = j >> 1;
-                uint32_t r[32];
+            for (int j = 0; j < 8; ++j) {                 // 16 columns at a time
+                const int hh = j >> 2;
+                uint32_t r[16];
                 if (c.first) {
 #pragma unroll
-                    for (int i2 = 0; i2 < 32; ++i2)
-                        r[i2] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 32 + i2) * kN) : 0.f);
+                    for (int i2 = 0; i2 < 16; ++i2)
+                        r[i2] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 16 + i2) * kN) : 0.f);
                 } else {
-                    tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
+                    tmem_ld16(tmem + lane_off + kColH + 16 * j, r);
                     tmem_wait_ld();
                 }
                 const float2 ep = hh ? ep1 : ep0, ed = hh ? ed1 : ed0;
                 const bool rn = hh ? rn1 : rn0;
 #pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2) {
+                for (int i2 = 0; i2 < 8; ++i2) {
                     // h entering the block (the cache values are h itself, eprev = 1 there)
                     const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep);
-                    packed[j * 16 + i2] = pack2(h);
+                    packed[j * 8 + i2] = pack2(h);
                     const float2 acc = rn ? __fmul2_rn(h, ed) : f2(r[2 * i2], r[2 * i2 + 1]);
                     r[2 * i2] = __float_as_uint(acc.x);
                     r[2 * i2 + 1] = __float_as_uint(acc.y);
                 }
-                if (write_tmem) tmem_st32(tmem + lane_off + kColH + 32 * j, r);
+                if (write_tmem) tmem_st16(tmem + lane_off + kColH + 16 * j, r);
             }
             if (write_tmem) tmem_wait_st();
             const float2 ef0 = make_float2(ar.eend[0], ar.eend[0]), ef1 = make_float2(ar.eend[1], ar.eend[1]);
