@@ -62,6 +62,7 @@ constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kHbufHead = 8192;    // one head of the half-n bf16 state copy: 64 rows x 128 B
 constexpr int kThreads = 512;     // 16 warps, each with exactly one role below
+constexpr uint32_t kArrBufs = 3;   // per-block decay arrays in flight (prepared two blocks ahead)
 
 constexpr uint64_t kSpinLimit = 4000000000ull;   // clock cycles (~2 s) per wait
 constexpr float kDiagFactorLimit = 80.f;         // |decay| of a 32-token block for the
@@ -90,7 +91,7 @@ struct Params {
     int32_t *device_status;
 };
 
-// per-block decay arrays, written by the Xw warps a block ahead
+// per-block decay arrays, written by the dt warp two blocks ahead
 //
 // The state is accumulated in TMEM in a scaled form hs = h exp(-R): a block
 // adds B^T (exp(E - cum_s) dt'_s x_s) with E = -R' and R' the scale in force
@@ -111,21 +112,18 @@ struct __align__(16) Arrays {
     float eend[2];         // exp(R after the block): hs after the block -> h
     int32_t renorm[2];     // renormalise the accumulator before this block
     int32_t exact[2][4];   // diagonal block needs the per-element path
-    float wtot[2][4];      // per 32-token block: sum of dt' A
-    float wmin[2][4];      // per 32-token block: extremes of its local cumsum
-    float wmax[2][4];
 };
 
 struct __align__(1024) Smem {
     uint8_t slot[kSlots][kTileBytes];     // TMA ring: C / B [n half][s][n], X [head][s][p]
     uint8_t xw[2][kHalfBytes];            // Xw (hi, then lo), [head][s][p], 128-B swizzle
     uint8_t hbuf[2 * kHbufHead];          // bf16 h, one half of n at a time: [head][n % 64][p]
-    Arrays arr[2];
+    Arrays arr[kArrBufs];
     uint64_t full[kSlots], empty[kSlots];
-    uint64_t arr_ready[2], arr_free[2], scan_bar[2];
+    uint64_t arr_ready[kArrBufs], arr_free[kArrBufs];
     uint64_t g_ready, s_ready, xhi_ready, xlo_ready, xbuf_free;
     uint64_t hs_a, hs_b, hbuf_a_done, state_ok, state_done;
-    uint64_t yinter_ready, y_scaled, y_ready, y_free[2], x_epi_done[2];
+    uint64_t yinter_ready, y_scaled, y_ready[2], y_free[2], x_epi_done[2];
     uint64_t drain_y, drain_h;
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -293,7 +291,7 @@ __device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t pari
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) || warp_wait_slow(sm, bar, parity, status);
 }
 
-__device__ __forceinline__ float softplus_f(float z) {
+__device__ __noinline__ float softplus_f(float z) {
     return fmaxf(z, 0.f) + log1pf(__expf(-fabsf(z)));
 }
 
@@ -359,17 +357,18 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16(v.x, v.y); }
 
-// S on a diagonal 32-token block whose decay is too steep for the factored
-// form: exp(cum_t - cum_s) dt'_s per element, G read from and S written back to
-// the 32 TMEM columns at taddr.  Rare; out of line.
-__device__ __noinline__ void s_diag_exact(uint32_t taddr, const Arrays &ar, int t, int j, float cum_t0,
+// S on the diagonal 32-token block when its decay is too steep for the
+// factored form: exp(cum_t - cum_s) dt'_s per element, for the 16 tokens s of
+// half-block c16; G is read from, and S_h written back to, the 16 TMEM columns
+// at taddr (head h at +8h).  Rare; out of line.
+__device__ __noinline__ void s_diag_exact(uint32_t taddr, const Arrays &ar, int t, int c16, float cum_t0,
                                           float cum_t1) {
-    uint32_t g[32], out0[16], out1[16];
-    tmem_ld32(taddr, g);
+    uint32_t g[16], out0[8], out1[8];
+    tmem_ld16(taddr, g);
     tmem_wait_ld();
 #pragma unroll
-    for (int i2 = 0; i2 < 16; ++i2) {
-        const int s = 32 * j + 2 * i2;
+    for (int i2 = 0; i2 < 8; ++i2) {
+        const int s = 16 * c16 + 2 * i2;
         float r0[2], r1[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -381,103 +380,92 @@ __device__ __noinline__ void s_diag_exact(uint32_t taddr, const Arrays &ar, int 
         out0[i2] = pack_bf16(r0[0], r0[1]);
         out1[i2] = pack_bf16(r1[0], r1[1]);
     }
-    tmem_st16(taddr, out0);
-    tmem_st16(taddr + 16, out1);
+    tmem_st8(taddr, out0);
+    tmem_st8(taddr + 8, out1);
 }
 
 // dt softplus, the within-block cumsum of dt' A and the per-block scales of one
-// block, computed by the four token warps (lane = token) into sm.arr[k & 1].
+// block, computed by one warp into sm.arr[k % kArrBufs]: four passes over the
+// 32-token sub-blocks, one token per lane, the cumsum carried across passes.
 // R0/R1 carry the running scale of the state accumulator per head (0 at the
-// first block of an item).  Out of line: one call site, shared code.
+// first block of an item).
 struct DtOut {
     float R0, R1;
     int32_t ok;
 };
-__device__ __noinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0, int32_t l, int32_t h0,
-                                      bool first, uint32_t k, float R0, float R1, int32_t *status) {
+__device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0, int32_t l, int32_t h0,
+                                         bool first, uint32_t k, float R0, float R1, int32_t *status) {
     const int lane = threadIdx.x & 31;
-    const int q = (threadIdx.x >> 5) - 4;
-    const int t = q * 32 + lane;
     DtOut out;
     out.R0 = first ? 0.f : R0;
     out.R1 = first ? 0.f : R1;
     out.ok = 0;
-    const int ab = k & 1;
+    const uint32_t ab = k % kArrBufs, use = k / kArrBufs;
     Arrays &ar = sm.arr[ab];
-    if (k >= 2 && !warp_wait(sm, &sm.arr_free[ab], ((k >> 1) - 1) & 1, status)) return out;
-    float d0 = 0.f, d1 = 0.f;
-    if (t < l) {
-        const float2 raw = *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + t) * p.H + h0);
-        const float z0 = raw.x + (p.dt_bias ? p.dt_bias[h0] : 0.f);
-        const float z1 = raw.y + (p.dt_bias ? p.dt_bias[h0 + 1] : 0.f);
-        d0 = p.dt_softplus ? softplus_f(z0) : z0;
-        d1 = p.dt_softplus ? softplus_f(z1) : z1;
-    }
-    float s0 = d0 * p.A[h0], s1 = d1 * p.A[h0 + 1];
+    const float bias0 = p.dt_bias ? p.dt_bias[h0] : 0.f, bias1 = p.dt_bias ? p.dt_bias[h0 + 1] : 0.f;
+    const float A0 = p.A[h0], A1 = p.A[h0 + 1];
+    // first pass's dt before the wait, so the load overlaps it
+    float2 raw = lane < l ? *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + lane) * p.H + h0)
+                          : make_float2(0.f, 0.f);
+    if (use > 0 && !warp_wait(sm, &sm.arr_free[ab], (use - 1) & 1, status)) return out;
+    float carry0 = 0.f, carry1 = 0.f;             // cum at the end of the previous sub-block
+    float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;
+#pragma unroll 1
+    for (int jb = 0; jb < 4; ++jb) {
+        const int tok = 32 * jb + lane;
+        const bool valid = tok < l;
+        // next pass's dt, loaded early
+        const int tn = tok + 32;
+        const float2 raw_next = (jb < 3 && tn < l)
+            ? *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + tn) * p.H + h0) : make_float2(0.f, 0.f);
+        const float z0 = raw.x + bias0, z1 = raw.y + bias1;
+        const float d0 = valid ? (p.dt_softplus ? softplus_f(z0) : z0) : 0.f;
+        const float d1 = valid ? (p.dt_softplus ? softplus_f(z1) : z1) : 0.f;
+        float s0 = d0 * A0, s1 = d1 * A1;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float v0 = __shfl_up_sync(0xffffffffu, s0, off);
-        const float v1 = __shfl_up_sync(0xffffffffu, s1, off);
-        if (lane >= off) { s0 += v0; s1 += v1; }
+        for (int off = 1; off < 32; off <<= 1) {
+            const float v0 = __shfl_up_sync(0xffffffffu, s0, off);
+            const float v1 = __shfl_up_sync(0xffffffffu, s1, off);
+            if (lane >= off) { s0 += v0; s1 += v1; }
+        }
+        const float c0 = carry0 + s0, c1 = carry1 + s1;
+        const float end0 = __shfl_sync(0xffffffffu, c0, 31), end1 = __shfl_sync(0xffffffffu, c1, 31);
+        ar.cum[0][tok] = c0;
+        ar.cum[1][tok] = c1;
+        ar.dtp[0][tok] = d0;
+        ar.dtp[1][tok] = d1;
+        ar.vfac[0][tok] = d0 != 0.f ? __expf(end0 - c0) * d0 : 0.f;
+        ar.vfac[1][tok] = d1 != 0.f ? __expf(end1 - c1) * d1 : 0.f;
+        ar.vdiag[0][tok] = d0 != 0.f ? __expf(fminf(carry0 - c0, kDiagFactorLimit)) * d0 : 0.f;
+        ar.vdiag[1][tok] = d1 != 0.f ? __expf(fminf(carry1 - c1, kDiagFactorLimit)) * d1 : 0.f;
+        lo0 = fminf(lo0, c0); hi0 = fmaxf(hi0, c0);
+        lo1 = fminf(lo1, c1); hi1 = fmaxf(hi1, c1);
+        if (lane == 0) {
+            ar.cumE[0][jb] = end0;
+            ar.cumE[1][jb] = end1;
+            ar.exact[0][jb] = fabsf(end0 - carry0) > kDiagFactorLimit;
+            ar.exact[1][jb] = fabsf(end1 - carry1) > kDiagFactorLimit;
+        }
+        carry0 = end0;
+        carry1 = end1;
+        raw = raw_next;
     }
-    // warp extremes of the local scan (the block's cum range follows from them)
-    float mn0 = s0, mx0 = s0, mn1 = s1, mx1 = s1;
+    // block extremes of cum (the exponent range of the scaled state inputs)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, off));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        lo0 = fminf(lo0, __shfl_xor_sync(0xffffffffu, lo0, off));
+        hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, off));
+        lo1 = fminf(lo1, __shfl_xor_sync(0xffffffffu, lo1, off));
+        hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, off));
     }
-    if (lane == 31) {
-        ar.wtot[0][q] = s0; ar.wtot[1][q] = s1;
-        ar.wmin[0][q] = mn0; ar.wmin[1][q] = mn1;
-        ar.wmax[0][q] = mx0; ar.wmax[1][q] = mx1;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.scan_bar[ab]);
-    if (!warp_wait(sm, &sm.scan_bar[ab], (k >> 1) & 1, status)) return out;
-    float cE[2][4], lo[2], hi[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        float run = 0.f;
-        lo[hh] = 0.f;
-        hi[hh] = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            lo[hh] = fminf(lo[hh], run + ar.wmin[hh][w]);
-            hi[hh] = fmaxf(hi[hh], run + ar.wmax[hh][w]);
-            run += ar.wtot[hh][w];
-            cE[hh][w] = run;
-        }
-    }
-    // cum before and at the end of this warp's 32-token block (static indices only)
-    float pre0 = 0.f, pre1 = 0.f, end0 = cE[0][0], end1 = cE[1][0];
-#pragma unroll
-    for (int w = 1; w < 4; ++w)
-        if (q == w) { pre0 = cE[0][w - 1]; pre1 = cE[1][w - 1]; end0 = cE[0][w]; end1 = cE[1][w]; }
-    const float c0 = s0 + pre0, c1 = s1 + pre1;
-    ar.cum[0][t] = c0;
-    ar.cum[1][t] = c1;
-    ar.dtp[0][t] = d0;
-    ar.dtp[1][t] = d1;
-    ar.vfac[0][t] = d0 != 0.f ? __expf(end0 - c0) * d0 : 0.f;
-    ar.vfac[1][t] = d1 != 0.f ? __expf(end1 - c1) * d1 : 0.f;
-    ar.vdiag[0][t] = d0 != 0.f ? __expf(fminf(pre0 - c0, kDiagFactorLimit)) * d0 : 0.f;
-    ar.vdiag[1][t] = d1 != 0.f ? __expf(fminf(pre1 - c1, kDiagFactorLimit)) * d1 : 0.f;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         float &R = hh ? out.R1 : out.R0;
-        const float dlt = cE[hh][3];
-        const bool fast = (-R - lo[hh] <= kScaleLimit) && (-R - hi[hh] >= -kScaleLimit);
+        const float dlt = hh ? carry1 : carry0;
+        const float lo = hh ? lo1 : lo0, hi = hh ? hi1 : hi0;
+        const bool fast = (-R - lo <= kScaleLimit) && (-R - hi >= -kScaleLimit);
         const float Rp = fast ? R : -dlt;          // scale in force for this block
-        if (t == 0) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                ar.cumE[hh][j] = cE[hh][j];
-                const float cb = j ? cE[hh][j - 1] : 0.f;
-                ar.exact[hh][j] = fabsf(cE[hh][j] - cb) > kDiagFactorLimit;
-            }
+        if (lane == 0) {
             ar.E[hh] = -Rp;
             ar.eprev[hh] = __expf(R);
             ar.edlt[hh] = __expf(dlt);
@@ -504,11 +492,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 2); }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.arr_ready[i], 4);
-            mbar_init(&sm.scan_bar[i], 4);
-            mbar_init(&sm.arr_free[i], 12);
             mbar_init(&sm.y_free[i], 4);
+            mbar_init(&sm.y_ready[i], 1);
             mbar_init(&sm.x_epi_done[i], 4);
+        }
+        for (uint32_t i = 0; i < kArrBufs; ++i) {
+            mbar_init(&sm.arr_ready[i], 1);
+            mbar_init(&sm.arr_free[i], 12);
         }
         mbar_init(&sm.g_ready, 1);
         mbar_init(&sm.s_ready, 4);
@@ -522,7 +512,6 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         mbar_init(&sm.state_done, 1);
         mbar_init(&sm.yinter_ready, 1);
         mbar_init(&sm.y_scaled, 4);
-        mbar_init(&sm.y_ready, 1);
         mbar_init(&sm.drain_y, 1);
         mbar_init(&sm.drain_h, 1);
         sm.abort_flag = 0;
@@ -551,6 +540,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             bool ok = true;
             while (ok && wk.next(p, c, false, true)) {
                 const int32_t row = c.row0;
+#pragma unroll 1
                 for (int j = 0; j < 3; ++j) {                    // C, B, X
                     const uint32_t tile = 3 * kc + j, slot = tile % kSlots, use = tile / kSlots;
                     const CUtensorMap *m = (j == 0) ? &map_c : (j == 1) ? &map_b : &map_x;
@@ -597,11 +587,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            wait_bar(sm, &sm.full[tB % kSlots], (tB / kSlots) & 1, status)))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    mma_ss(tmem + kColG, smem_desc_sw128(bC + off, 16, 1024),
-                           smem_desc_sw128(bB + off, 16, 1024), kIdG, ks > 0);
+                {
+                    const uint64_t dc = smem_desc_sw128(bC, 16, 1024), db = smem_desc_sw128(bB, 16, 1024);
+#pragma unroll 1
+                    for (uint32_t ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + kColG, dc + off, db + off, kIdG, ks > 0);
+                    }
                 }
                 mma_commit(&sm.g_ready);
                 mma_commit(&sm.empty[tB % kSlots]);              // this path's only read of B
@@ -610,18 +602,22 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            (kc < 2 || wait_bar(sm, &sm.y_free[kc & 1], ((kc >> 1) - 1) & 1, status))))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tmem + ycol, smem_desc_sw128(bC + ks * 32, 16, 1024),
-                           smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, ks > 0);
+                {
+                    const uint64_t dc = smem_desc_sw128(bC, 16, 1024), dh = smem_desc_sw128(bH, kHbufHead, 1024);
+#pragma unroll 1
+                    for (uint32_t ks = 0; ks < 4; ++ks)
+                        mma_ss(tmem + ycol, dc + ks * 2, dh + ks * 128, kIdY, ks > 0);
+                }
                 mma_commit(&sm.hbuf_a_done);
                 // ---- Y[b] += C h^T, second half of n ----
                 if (!(ok = wait_bar(sm, &sm.hs_b, kc & 1, status))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tmem + ycol, smem_desc_sw128(bC + kHalfBytes + ks * 32, 16, 1024),
-                           smem_desc_sw128(bH + ks * 2048, kHbufHead, 1024), kIdY, 1);
+                {
+                    const uint64_t dc = smem_desc_sw128(bC + kHalfBytes, 16, 1024), dh = smem_desc_sw128(bH, kHbufHead, 1024);
+#pragma unroll 1
+                    for (uint32_t ks = 0; ks < 4; ++ks)
+                        mma_ss(tmem + ycol, dc + ks * 2, dh + ks * 128, kIdY, 1);
+                }
                 mma_commit(&sm.yinter_ready);
                 mma_commit(&sm.empty[tC % kSlots]);
                 mma_commit(&sm.empty[tC % kSlots]);
@@ -631,16 +627,16 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            wait_bar(sm, &sm.y_scaled, kc & 1, status)))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t acol = kColG + 32 * (ks >> 1) + 16 * hh + 8 * (ks & 1);
-                        mma_ts(tmem + ycol + 64 * hh, tmem + acol,
-                               smem_desc_sw128(bX + hh * kHalfBytes + ks * 2048, 1024, 1024), kIdSX, 1);
+                {
+                    const uint64_t dx = smem_desc_sw128(bX, 1024, 1024);
+#pragma unroll 1
+                    for (uint32_t i = 0; i < 16; ++i) {
+                        const uint32_t hh = i >> 3, ks = i & 7;
+                        const uint32_t acol = kColG + 16 * ks + 8 * hh;     // S_h, tokens 16ks..16ks+15
+                        mma_ts(tmem + ycol + 64 * hh, tmem + acol, dx + ((hh * kHalfBytes + ks * 2048) >> 4), kIdSX, 1);
                     }
                 }
-                mma_commit(&sm.y_ready);
+                mma_commit(&sm.y_ready[kc & 1]);
                 mma_commit(&sm.empty[tX % kSlots]);
                 ++kc;
             }
@@ -664,18 +660,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                            wait_bar(sm, &sm.state_ok, kc & 1, status)))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
-                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
+                const uint64_t db = smem_desc_sw128(bB, kHalfBytes, 1024), dw = smem_desc_sw128(bW, kHalfBytes, 1024);
+#pragma unroll 1
+                for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
                 mma_commit(&sm.xbuf_free);
                 // ---- hs += B^T Xw_lo ----
                 if (!(ok = wait_bar(sm, &sm.xlo_ready, kc & 1, status))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tmem + kColH, smem_desc_sw128(bB + ks * 2048, kHalfBytes, 1024),
-                           smem_desc_sw128(bW + ks * 2048, kHalfBytes, 1024), kIdH, 1);
+#pragma unroll 1
+                for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
                 mma_commit(&sm.state_done);
                 mma_commit(&sm.xbuf_free);
                 mma_commit(&sm.empty[tB % kSlots]);
@@ -685,96 +678,86 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             mma_commit(&sm.drain_h);
             wait_bar(sm, &sm.drain_h, 0, nullptr);
         }
+      } else {
+        // ===================== dt warp (also owns the TMEM allocation) =====================
+        Walker wk;
+        Chunk c;
+        uint32_t k = 0;
+        DtOut ds;
+        ds.R0 = ds.R1 = 0.f;
+        ds.ok = 1;
+        while (ds.ok && wk.next(p, c, false)) {
+            ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, k, ds.R0, ds.R1, status);
+            ++k;
+        }
       }
-      // warp 2: TMEM owner only (allocates above, frees after the final barrier)
     } else if (warp >= 4 && warp < 8) {
-        // ===================== dt, scales and the scaled Xw (lane = token) =====================
-        // Per block k (once X lands): the dt arrays of block k+1, then the hi
-        // part of Xw into the Xw buffer once block k-1's state MMAs have read it,
-        // then the lo part once the hi MMA has read it.
+        // ===================== scaled Xw (lane = token) =====================
+        // Per block k, with w_s = exp(E - cum_s) dt'_s: the hi part bf16(w x) into
+        // the Xw buffer once block k-1's lo MMA has read it, then the lo part
+        // bf16(w x - hi) once the hi MMA has.  Compact loops: the hot code of all
+        // roles together has to stay within the SM's instruction cache.
         const int q = warp - 4;
         const int t = q * 32 + lane;
         Walker wk;
         Chunk c;
-        bool have_cur = wk.next(p, c, false);
-        int32_t cur_l = c.l;                      // valid tokens of the block being filled
         uint32_t kc = 0;
         bool ok = true;
-        DtOut ds;                                 // running scale of the state accumulator
-        ds.R0 = ds.R1 = 0.f;
-        ds.ok = 1;
-        if (have_cur) {
-            ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, 0, ds.R0, ds.R1, status);
-            ok = ds.ok != 0;
-        }
-        while (ok && have_cur) {
-            const int ab = kc & 1;
+        while (ok && wk.next(p, c, false)) {
+            const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
             const uint32_t tX = 3 * kc + 2;
             const uint8_t *xt = sm.slot[tX % kSlots];
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status) &&
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status) &&
                        warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status)))
                 break;
-            const float w0 = (t < cur_l) ? __expf(ar.E[0] - ar.cum[0][t]) * ar.dtp[0][t] : 0.f;
-            const float w1 = (t < cur_l) ? __expf(ar.E[1] - ar.cum[1][t]) * ar.dtp[1][t] : 0.f;
+            const float w0 = (t < c.l) ? __expf(ar.E[0] - ar.cum[0][t]) * ar.dtp[0][t] : 0.f;
+            const float w1 = (t < c.l) ? __expf(ar.E[1] - ar.cum[1][t]) * ar.dtp[1][t] : 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
-            // ---- dt of the next block while the previous block's state MMAs run ----
-            const bool have_nxt = wk.next(p, c, false);
-            if (have_nxt) {
-                ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, kc + 1, ds.R0, ds.R1, status);
-                if (!(ok = ds.ok != 0)) break;
-            }
-            const int32_t nxt_l = c.l;
-            // ---- hi part into the buffer once those MMAs have read it ----
+            // ---- hi part bf16(w x) into the buffer once block k-1's lo MMA has read it ----
             if (kc > 0 && !(ok = warp_wait(sm, &sm.xbuf_free, 1, status))) break;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+            for (int i = 0; i < 16; ++i) {
+                const int hh = i >> 3, cc = i & 7;
                 const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
-#pragma unroll 2
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
-                    uint4 o;
-                    o.x = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.x), bf16_hi(xv.x))));
-                    o.y = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.y), bf16_hi(xv.y))));
-                    o.z = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.z), bf16_hi(xv.z))));
-                    o.w = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.w), bf16_hi(xv.w))));
-                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = o;
-                }
+                const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                uint4 o;
+                o.x = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.x), bf16_hi(xv.x))));
+                o.y = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.y), bf16_hi(xv.y))));
+                o.z = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.z), bf16_hi(xv.z))));
+                o.w = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.w), bf16_hi(xv.w))));
+                *reinterpret_cast<uint4 *>(sm.xw[0] + off) = o;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.xhi_ready);
-            // ---- lo part = bf16(w x - hi) into the buffer once the hi MMA has read it ----
+            // ---- lo part bf16(w x - hi) once the hi MMA has read the buffer ----
             if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+            for (int i = 0; i < 16; ++i) {
+                const int hh = i >> 3, cc = i & 7;
                 const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
-#pragma unroll 2
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
-                    const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
-                    uint32_t o[4];
+                const uint32_t off = hh * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4);
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xt + off);
+                const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
+                uint32_t o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
-                        const uint32_t h2 = pack2(v);
-                        o[e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(h2), -bf16_hi(h2))));
-                    }
-                    *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v = __fmul2_rn(ww, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])));
+                    const uint32_t h2 = pack2(v);
+                    o[e] = pack2(__fadd2_rn(v, make_float2(-bf16_lo(h2), -bf16_hi(h2))));
                 }
+                *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.xlo_ready);
-            have_cur = have_nxt;
-            cur_l = nxt_l;
             ++kc;
         }
     } else if (warp >= 8 && warp < 12) {
-        // ===================== S, row scaling, epilogue (lane = token) =====================
+        // ===================== S and row scaling (lane = token) =====================
         const int q = warp - 8;
         const int t = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -782,59 +765,70 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
-        __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.out_y);
         while (ok && wk.next(p, c, false)) {
-            const int ab = kc & 1;
+            const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
             const uint32_t ycol = kColY + 128 * (kc & 1);
-            const uint8_t *xt = sm.slot[(3 * kc + 2) % kSlots];
             // ---- S_h from G, in place ----
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status) &&
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status) &&
                        warp_wait(sm, &sm.g_ready, kc & 1, status)))
                 break;
             tc_fence_after();
             const float cum_t0 = ar.cum[0][t], cum_t1 = ar.cum[1][t];
+            // 16 G columns (tokens s) at a time; the 8 packed columns of each head
+            // go back into the 16 just read (head h at +8h).
+            // exp(cum_t - cum_s) = exp(cum_t - c_b) exp(c_b - cum_s): below the
+            // diagonal 32-token block c_b is the end of the block of s (both
+            // factors <= 1), on it the start (first factor <= 1, second <=
+            // exp(kDiagFactorLimit)); the second factor times dt'_s is per token.
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t taddr = tmem + lane_off + kColG + 32 * j;
-                if (j == q && (ar.exact[0][j] || ar.exact[1][j])) {
-                    s_diag_exact(taddr, ar, t, j, cum_t0, cum_t1);   // steep decay: rare
+            for (int c16 = 0; c16 < 8; ++c16) {
+                const int j = c16 >> 1;
+                const uint32_t taddr = tmem + lane_off + kColG + 16 * c16;
+                uint32_t out0[8], out1[8];
+                if (j > q) {                                  // above the diagonal: S = 0
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) out0[i2] = 0u;
+                    tmem_st8(taddr, out0);
+                    tmem_st8(taddr + 8, out0);
                     continue;
                 }
-                // exp(cum_t - cum_s) = exp(cum_t - c_b) exp(c_b - cum_s): below the
-                // diagonal c_b is the end of block j (both factors <= 1), on it the
-                // start of the block (first factor <= 1, second <= exp(kDiagFactorLimit));
-                // the second factor times dt'_s is precomputed per token.  One code
-                // path for every j: tokens s at or beyond `lim` (causal mask, or the
-                // whole block above the diagonal) are selected to 0.
-                uint32_t g[32], out0[16], out1[16];
-                tmem_ld32(taddr, g);
                 const bool diag = (j == q);
-                const int lim = j < q ? 32 : (diag ? t - 32 * j + 1 : 0);
+                if (diag && (ar.exact[0][j] || ar.exact[1][j])) {
+                    s_diag_exact(taddr, ar, t, c16, cum_t0, cum_t1);   // steep decay: rare
+                    continue;
+                }
+                uint32_t g[16];
+                tmem_ld16(taddr, g);
                 const float b0 = diag ? (j ? ar.cumE[0][j - 1] : 0.f) : ar.cumE[0][j];
                 const float b1 = diag ? (j ? ar.cumE[1][j - 1] : 0.f) : ar.cumE[1][j];
-                const float *v0p = (diag ? ar.vdiag[0] : ar.vfac[0]) + 32 * j;
-                const float *v1p = (diag ? ar.vdiag[1] : ar.vfac[1]) + 32 * j;
+                const float *v0p = (diag ? ar.vdiag[0] : ar.vfac[0]) + 16 * c16;
+                const float *v1p = (diag ? ar.vdiag[1] : ar.vfac[1]) + 16 * c16;
+                const int lim = diag ? t - 16 * c16 + 1 : 16;    // causal mask: s - 16 c16 < lim
                 const float u0 = __expf(cum_t0 - b0), u1 = __expf(cum_t1 - b1);
                 const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2) {
-                    const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
-                    const float2 v0 = *reinterpret_cast<const float2 *>(v0p + 2 * i2);
-                    const float2 v1 = *reinterpret_cast<const float2 *>(v1p + 2 * i2);
-                    float2 r0 = __fmul2_rn(__fmul2_rn(gg, uu0), v0);
-                    float2 r1 = __fmul2_rn(__fmul2_rn(gg, uu1), v1);
-                    const bool kx = 2 * i2 < lim, ky = 2 * i2 + 1 < lim;
-                    r0.x = kx ? r0.x : 0.f;
-                    r1.x = kx ? r1.x : 0.f;
-                    r0.y = ky ? r0.y : 0.f;
-                    r1.y = ky ? r1.y : 0.f;
-                    out0[i2] = pack2(r0);
-                    out1[i2] = pack2(r1);
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    const float4 va = *reinterpret_cast<const float4 *>(v0p + 4 * i4);
+                    const float4 vb = *reinterpret_cast<const float4 *>(v1p + 4 * i4);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i2 = 2 * i4 + e;
+                        const float2 gg = f2(g[2 * i2], g[2 * i2 + 1]);
+                        float2 r0 = __fmul2_rn(__fmul2_rn(gg, uu0), e ? make_float2(va.z, va.w) : make_float2(va.x, va.y));
+                        float2 r1 = __fmul2_rn(__fmul2_rn(gg, uu1), e ? make_float2(vb.z, vb.w) : make_float2(vb.x, vb.y));
+                        const bool kx = 2 * i2 < lim, ky = 2 * i2 + 1 < lim;
+                        r0.x = kx ? r0.x : 0.f;
+                        r1.x = kx ? r1.x : 0.f;
+                        r0.y = ky ? r0.y : 0.f;
+                        r1.y = ky ? r1.y : 0.f;
+                        out0[i2] = pack2(r0);
+                        out1[i2] = pack2(r1);
+                    }
                 }
-                tmem_st16(taddr, out0);
-                tmem_st16(taddr + 16, out1);
+                tmem_st8(taddr, out0);
+                tmem_st8(taddr + 8, out1);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -848,66 +842,33 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (!(ok = warp_wait(sm, &sm.yinter_ready, kc & 1, status))) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
+            for (int c16 = 0; c16 < 8; ++c16) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_off + ycol + 16 * c16, r);
+                const float2 ee = (c16 >> 2) ? make_float2(e1, e1) : make_float2(e0, e0);
                 tmem_wait_ld();
-                const float2 ee = (j >> 1) ? make_float2(e1, e1) : make_float2(e0, e0);
 #pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2) {
+                for (int i2 = 0; i2 < 8; ++i2) {
                     const float2 v = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ee);
                     r[2 * i2] = __float_as_uint(v.x);
                     r[2 * i2 + 1] = __float_as_uint(v.y);
                 }
-                tmem_st32(tmem + lane_off + ycol + 32 * j, r);
+                tmem_st16(tmem + lane_off + ycol + 16 * c16, r);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.y_scaled);
-            // ---- y = Y + D x (x from the smem tile, which stays until x_epi_done) ----
-            const bool valid = t < c.l;
-            const int64_t grow = (int64_t)(c.row0 + t) * p.H * kP + (int64_t)c.h0 * kP;
-            const float D0 = p.D ? p.D[c.h0] : 0.f, D1 = p.D ? p.D[c.h0 + 1] : 0.f;
-            if (!(ok = warp_wait(sm, &sm.y_ready, kc & 1, status))) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + ycol + 32 * j, r);
-                tmem_wait_ld();
-                if (j == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.y_free[kc & 1]);
-                }
-                const int hh = j >> 1;
-                const float2 dd = hh ? make_float2(D1, D1) : make_float2(D0, D0);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int chunk = (j & 1) * 4 + cc;
-                    const uint4 x4 = *reinterpret_cast<const uint4 *>(
-                        xt + hh * kHalfBytes + t * 128 + ((chunk ^ (t & 7)) << 4));
-                    const uint32_t xw4[4] = {x4.x, x4.y, x4.z, x4.w};
-                    uint32_t yw[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        yw[e] = pack2(__ffma2_rn(dd, make_float2(bf16_lo(xw4[e]), bf16_hi(xw4[e])),
-                                                 f2(r[cc * 8 + 2 * e], r[cc * 8 + 2 * e + 1])));
-                    if (valid)
-                        reinterpret_cast<uint4 *>(yg + grow)[j * 4 + cc] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.x_epi_done[kc & 1]);
             ++kc;
         }
     } else if (warp >= 12) {
         // ===================== state (lane = state column n) =====================
         // The accumulator holds hs = h exp(-R).  Per block this role reads hs
-        // (renormalising it when the dt warp asks), writes the bf16 copy of h for
+        // (renormalising it when the block's scales ask for it), writes the bf16 copy of h for
         // C h^T -- warps 12-13 own n < 64, warps 14-15 n >= 64, matching the two
-        // halves of that MMA -- and stores the final state of each item.
+        // halves of that MMA -- and stores the final state of each item.  While a
+        // block's state MMAs run it also writes y of the previous block (lane =
+        // token there).
         const int q = warp - 12;
         const int n = q * 32 + lane;
         const bool first_half = q < 2;
@@ -918,7 +879,53 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         uint32_t kc = 0;
         bool ok = true;
         StT *cache = static_cast<StT *>(p.state_cache);
-        uint32_t packed[64];                      // bf16 copy of this lane's 128 state values
+        int32_t prev_row0 = 0, prev_l = 0, prev_h0 = 0;   // previous block, for its y epilogue
+        // y = Y + D x of block k (lane = token t here; x from the smem tile, which
+        // stays until x_epi_done), run while block k+1's state MMAs execute
+        auto epilogue = [&](uint32_t k) -> bool {
+            const int t = n;
+            const uint32_t ycol = kColY + 128 * (k & 1);
+            const uint8_t *xt = sm.slot[(3 * k + 2) % kSlots];
+            const bool valid = t < prev_l;
+            __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(p.out_y) +
+                                  ((int64_t)(prev_row0 + t) * p.H + prev_h0) * kP;
+            const float D0 = p.D ? p.D[prev_h0] : 0.f, D1 = p.D ? p.D[prev_h0 + 1] : 0.f;
+            // double buffered: block k+1's Y can be final before this check
+            if (!warp_wait(sm, &sm.y_ready[k & 1], (k >> 1) & 1, status)) return false;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c16 = 0; c16 < 8; ++c16) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_off + ycol + 16 * c16, r);
+                const int hh = c16 >> 2;
+                const float2 dd = hh ? make_float2(D1, D1) : make_float2(D0, D0);
+                // x of this head and these 16 p: two 16-byte chunks of the swizzled row
+                const int ch = (c16 & 3) * 2;
+                const uint8_t *xrow = xt + hh * kHalfBytes + t * 128;
+                const uint4 xa = *reinterpret_cast<const uint4 *>(xrow + ((ch ^ (t & 7)) << 4));
+                const uint4 xb = *reinterpret_cast<const uint4 *>(xrow + (((ch + 1) ^ (t & 7)) << 4));
+                tmem_wait_ld();
+                if (c16 == 7) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.y_free[k & 1]);
+                }
+                const uint32_t xw8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                uint32_t yw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    yw[e] = pack2(__ffma2_rn(dd, make_float2(bf16_lo(xw8[e]), bf16_hi(xw8[e])),
+                                             f2(r[2 * e], r[2 * e + 1])));
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow) + hh * 8 + ch;
+                    dst[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                    dst[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.x_epi_done[k & 1]);
+            return true;
+        };
         while (ok && wk.next(p, c, true)) {
             const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
             if (c.empty_item) {
@@ -930,45 +937,61 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 }
                 continue;
             }
-            const int ab = kc & 1;
+            const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc >> 1) & 1, status))) break;
+            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status))) break;
             if (!c.first) {
                 if (!(ok = warp_wait(sm, &sm.state_done, (kc - 1) & 1, status))) break;
                 tc_fence_after();
+            } else {
+                // the item's initial state (or zeros) into the accumulator columns
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        r[i] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 16 + i) * kN) : 0.f);
+                    tmem_st16(tmem + lane_off + kColH + 16 * j, r);
+                }
+                tmem_wait_st();
             }
+            uint32_t packed[64];                  // bf16 copy of this lane's 128 state values
             // per head: the state entering the block is hs * eprev; renormalised
             // accumulators hold exp(dlt) h instead
             const float2 ep0 = make_float2(ar.eprev[0], ar.eprev[0]), ep1 = make_float2(ar.eprev[1], ar.eprev[1]);
-            const float2 ed0 = make_float2(ar.edlt[0], ar.edlt[0]), ed1 = make_float2(ar.edlt[1], ar.edlt[1]);
             const bool rn0 = ar.renorm[0] != 0, rn1 = ar.renorm[1] != 0;
-            const bool write_tmem = c.first || rn0 || rn1;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {                 // 16 columns at a time
-                const int hh = j >> 2;
                 uint32_t r[16];
-                if (c.first) {
+                tmem_ld16(tmem + lane_off + kColH + 16 * j, r);
+                tmem_wait_ld();
+                const float2 ep = (j >> 2) ? ep1 : ep0;
 #pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2)
-                        r[i2] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 16 + i2) * kN) : 0.f);
-                } else {
+                for (int i2 = 0; i2 < 8; ++i2)       // h entering the block (eprev = 1 at an item's first block)
+                    packed[j * 8 + i2] = pack2(__fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep));
+            }
+            if (rn0 || rn1) {
+                // renormalise the accumulator to exp(dlt) h (rare: the block's exponents
+                // left the range of the running scale)
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    const int hh = j >> 2;
+                    if (!(hh ? rn1 : rn0)) continue;
+                    const float2 f = hh ? make_float2(ar.eprev[1] * ar.edlt[1], ar.eprev[1] * ar.edlt[1])
+                                        : make_float2(ar.eprev[0] * ar.edlt[0], ar.eprev[0] * ar.edlt[0]);
+                    uint32_t r[16];
                     tmem_ld16(tmem + lane_off + kColH + 16 * j, r);
                     tmem_wait_ld();
-                }
-                const float2 ep = hh ? ep1 : ep0, ed = hh ? ed1 : ed0;
-                const bool rn = hh ? rn1 : rn0;
 #pragma unroll
-                for (int i2 = 0; i2 < 8; ++i2) {
-                    // h entering the block (the cache values are h itself, eprev = 1 there)
-                    const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep);
-                    packed[j * 8 + i2] = pack2(h);
-                    const float2 acc = rn ? __fmul2_rn(h, ed) : f2(r[2 * i2], r[2 * i2 + 1]);
-                    r[2 * i2] = __float_as_uint(acc.x);
-                    r[2 * i2 + 1] = __float_as_uint(acc.y);
+                    for (int i2 = 0; i2 < 8; ++i2) {
+                        const float2 v = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), f);
+                        r[2 * i2] = __float_as_uint(v.x);
+                        r[2 * i2 + 1] = __float_as_uint(v.y);
+                    }
+                    tmem_st16(tmem + lane_off + kColH + 16 * j, r);
                 }
-                if (write_tmem) tmem_st16(tmem + lane_off + kColH + 16 * j, r);
+                tmem_wait_st();
             }
-            if (write_tmem) tmem_wait_st();
             const float2 ef0 = make_float2(ar.eend[0], ar.eend[0]), ef1 = make_float2(ar.eend[1], ar.eend[1]);
             tc_fence_before();
             __syncwarp();
@@ -994,6 +1017,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(first_half ? &sm.hs_a : &sm.hs_b);
+            // ---- y of the previous block ----
+            if (kc > 0 && !(ok = epilogue(kc - 1))) break;
+            prev_row0 = c.row0;
+            prev_l = c.l;
+            prev_h0 = c.h0;
             if (c.last) {
                 // final state of the item: h = hs * exp(R after the block)
                 if (!(ok = warp_wait(sm, &sm.state_done, kc & 1, status))) break;
@@ -1017,6 +1045,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             }
             ++kc;
         }
+        if (ok && kc > 0) epilogue(kc - 1);       // y of the last block
     }
 
     tc_fence_before();
