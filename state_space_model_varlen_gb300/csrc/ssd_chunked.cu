@@ -387,13 +387,32 @@ __device__ __noinline__ void s_diag_exact(uint32_t taddr, const Arrays &ar, int 
 // dt softplus, the within-block cumsum of dt' A and the per-block scales of one
 // block, computed by one warp into sm.arr[k % kArrBufs]: four passes over the
 // 32-token sub-blocks, one token per lane, the cumsum carried across passes.
+// The block's dt values come in `dr`, loaded a block earlier by the caller.
 // R0/R1 carry the running scale of the state accumulator per head (0 at the
 // first block of an item).
 struct DtOut {
     float R0, R1;
     int32_t ok;
 };
-__device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0, int32_t l, int32_t h0,
+// dt of tokens 32 jb + lane (jb = 0..3) of a block, heads h0 and h0 + 1.
+struct DtRaw {
+    float2 v0, v1, v2, v3;
+};
+__device__ __forceinline__ DtRaw dt_load(const Params &p, int32_t row0, int32_t l, int32_t h0) {
+    const int lane = threadIdx.x & 31;
+    auto ld = [&](int jb) {
+        const int tok = 32 * jb + lane;
+        return tok < l ? __ldg(reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + tok) * p.H + h0))
+                       : make_float2(0.f, 0.f);
+    };
+    DtRaw d;
+    d.v0 = ld(0);
+    d.v1 = ld(1);
+    d.v2 = ld(2);
+    d.v3 = ld(3);
+    return d;
+}
+__device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, const DtRaw &dr, int32_t l, int32_t h0,
                                          bool first, uint32_t k, float R0, float R1, int32_t *status) {
     const int lane = threadIdx.x & 31;
     DtOut out;
@@ -404,9 +423,6 @@ __device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0
     Arrays &ar = sm.arr[ab];
     const float bias0 = p.dt_bias ? p.dt_bias[h0] : 0.f, bias1 = p.dt_bias ? p.dt_bias[h0 + 1] : 0.f;
     const float A0 = p.A[h0], A1 = p.A[h0 + 1];
-    // first pass's dt before the wait, so the load overlaps it
-    float2 raw = lane < l ? *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + lane) * p.H + h0)
-                          : make_float2(0.f, 0.f);
     if (use > 0 && !warp_wait(sm, &sm.arr_free[ab], (use - 1) & 1, status)) return out;
     float carry0 = 0.f, carry1 = 0.f;             // cum at the end of the previous sub-block
     float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;
@@ -414,10 +430,7 @@ __device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0
     for (int jb = 0; jb < 4; ++jb) {
         const int tok = 32 * jb + lane;
         const bool valid = tok < l;
-        // next pass's dt, loaded early
-        const int tn = tok + 32;
-        const float2 raw_next = (jb < 3 && tn < l)
-            ? *reinterpret_cast<const float2 *>(p.dt + (int64_t)(row0 + tn) * p.H + h0) : make_float2(0.f, 0.f);
+        const float2 raw = jb == 0 ? dr.v0 : jb == 1 ? dr.v1 : jb == 2 ? dr.v2 : dr.v3;
         const float z0 = raw.x + bias0, z1 = raw.y + bias1;
         const float d0 = valid ? (p.dt_softplus ? softplus_f(z0) : z0) : 0.f;
         const float d1 = valid ? (p.dt_softplus ? softplus_f(z1) : z1) : 0.f;
@@ -448,7 +461,6 @@ __device__ __forceinline__ DtOut dt_prep(Smem &sm, const Params &p, int32_t row0
         }
         carry0 = end0;
         carry1 = end1;
-        raw = raw_next;
     }
     // block extremes of cum (the exponent range of the scaled state inputs)
 #pragma unroll
@@ -681,14 +693,21 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
       } else {
         // ===================== dt warp (also owns the TMEM allocation) =====================
         Walker wk;
-        Chunk c;
+        Chunk c, cn;
         uint32_t k = 0;
         DtOut ds;
         ds.R0 = ds.R1 = 0.f;
         ds.ok = 1;
-        while (ds.ok && wk.next(p, c, false)) {
-            ds = dt_prep(sm, p, c.row0, c.l, c.h0, c.first, k, ds.R0, ds.R1, status);
+        bool have = wk.next(p, c, false);
+        DtRaw dr = have ? dt_load(p, c.row0, c.l, c.h0) : DtRaw{};
+        while (ds.ok && have) {
+            const bool have_n = wk.next(p, cn, false);
+            const DtRaw drn = have_n ? dt_load(p, cn.row0, cn.l, cn.h0) : DtRaw{};   // next block's dt, early
+            ds = dt_prep(sm, p, dr, c.l, c.h0, c.first, k, ds.R0, ds.R1, status);
             ++k;
+            c = cn;
+            dr = drn;
+            have = have_n;
         }
       }
     } else if (warp >= 4 && warp < 8) {
