@@ -26,18 +26,25 @@
 //                                          Xw split into bf16 hi + lo
 //   The hi/lo split keeps the state contributions accurate to ~2^-16, so final
 //   states meet fp32-storage accuracy; the y path runs on bf16 operands with
-//   fp32 accumulation.  Y is double buffered in TMEM so block k+1's C h^T can
-//   start while block k's epilogue drains.
+//   fp32 accumulation.  The state is accumulated in a scaled form with a
+//   running per-head scale, so a block needs no rescaling pass over it.  Y is
+//   double buffered in TMEM so block k+1's C h^T can start while block k's
+//   epilogue drains.
 //
-// Warp roles (16 warps): warp 0 TMA producer; warp 1 issues the output-path
-// MMAs (G, C h^T, S X) and warp 3 the state-path MMAs (B^T Xw), so neither
-// path waits behind the other; warp 2 owns the TMEM allocation; warps 4-7
-// (lane = token) compute dt softplus, the within-block cumsum and the state
-// scales a block ahead and build the scaled Xw; warps 8-11 build S, scale the
-// rows of Y and write y (lane = token); warps 12-15 own the state (lane = state column n: bf16 copy for
-// C h^T, occasional renormalisation, cache I/O).  All hand-offs are
-// mbarriers; every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT
-// in device_status instead of hanging.
+// Warp roles (16 warps): warp 0 TMA producer (C, B, X tiles of 128 tokens,
+// 5-slot ring); warp 1 issues the output-path MMAs (G, C h^T, S X); warp 2
+// owns the TMEM allocation and computes dt softplus, the within-block cumsum
+// and the state scales two blocks ahead; warps 4-7 (lane = token) build the
+// scaled Xw and issue the state MMAs (B^T Xw); warps 8-11 (lane = token) build
+// S and scale the rows of Y; warps 12-15 own the state (lane = state column n:
+// bf16 copy for C h^T, cache I/O) and write y of the previous block; warp 3 has
+// no role.  Hand-offs are mbarriers (and one named barrier inside warps 4-7);
+// every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT in
+// device_status instead of hanging.
+//
+// The hot loops are compact (little unrolling): with sixteen warps in six roles
+// the kernel's instruction footprint, not its arithmetic, set the block time
+// when the loops were unrolled.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -121,7 +128,7 @@ struct __align__(1024) Smem {
     Arrays arr[kArrBufs];
     uint64_t full[kSlots], empty[kSlots];
     uint64_t arr_ready[kArrBufs], arr_free[kArrBufs];
-    uint64_t g_ready, s_ready, xhi_ready, xlo_ready, xbuf_free;
+    uint64_t g_ready, s_ready, xbuf_free;
     uint64_t hs_a, hs_b, hbuf_a_done, state_ok, state_done;
     uint64_t yinter_ready, y_scaled, y_ready[2], y_free[2], x_epi_done[2];
     uint64_t drain_y, drain_h;
@@ -289,6 +296,16 @@ __device__ __noinline__ bool warp_wait_slow(Smem &sm, uint64_t *bar, uint32_t pa
 // this kernel, so once one lane observes completion every lane will.
 __device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) || warp_wait_slow(sm, bar, parity, status);
+}
+
+// Barrier over the four Xw warps (named barrier 1) that also ANDs a flag over
+// them, so that the group takes every exit together.
+__device__ __forceinline__ bool xw_group_and(bool v) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v) : "memory");
+    return r != 0;
 }
 
 __device__ __noinline__ float softplus_f(float z) {
@@ -514,8 +531,6 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         }
         mbar_init(&sm.g_ready, 1);
         mbar_init(&sm.s_ready, 4);
-        mbar_init(&sm.xhi_ready, 4);
-        mbar_init(&sm.xlo_ready, 4);
         mbar_init(&sm.xbuf_free, 1);
         mbar_init(&sm.hs_a, 2);
         mbar_init(&sm.hs_b, 2);
@@ -656,40 +671,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             wait_bar(sm, &sm.drain_y, 0, nullptr);
         }
     } else if (warp == 3) {
-        // ===================== MMA issuer, state path =====================
-        if (lane == 0) {
-            Walker wk;
-            Chunk c;
-            uint32_t kc = 0;
-            bool ok = true;
-            const uint32_t bW = smem_u32(sm.xw[0]);
-            while (ok && wk.next(p, c, false)) {
-                const uint32_t tB = 3 * kc + 1, tX = 3 * kc + 2;
-                const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
-                // ---- hs += B^T Xw_hi ----
-                if (!(ok = wait_bar(sm, &sm.full[tB % kSlots], (tB / kSlots) & 1, status) &&
-                           wait_bar(sm, &sm.xhi_ready, kc & 1, status) &&
-                           wait_bar(sm, &sm.state_ok, kc & 1, status)))
-                    break;
-                tc_fence_after();
-                const uint64_t db = smem_desc_sw128(bB, kHalfBytes, 1024), dw = smem_desc_sw128(bW, kHalfBytes, 1024);
-#pragma unroll 1
-                for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
-                mma_commit(&sm.xbuf_free);
-                // ---- hs += B^T Xw_lo ----
-                if (!(ok = wait_bar(sm, &sm.xlo_ready, kc & 1, status))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
-                mma_commit(&sm.state_done);
-                mma_commit(&sm.xbuf_free);
-                mma_commit(&sm.empty[tB % kSlots]);
-                mma_commit(&sm.empty[tX % kSlots]);              // the Xw passes have read X
-                ++kc;
-            }
-            mma_commit(&sm.drain_h);
-            wait_bar(sm, &sm.drain_h, 0, nullptr);
-        }
+        // no role: the state MMAs are issued from the Xw warps
       } else {
         // ===================== dt warp (also owns the TMEM allocation) =====================
         Walker wk;
@@ -714,28 +696,31 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         // ===================== scaled Xw (lane = token) =====================
         // Per block k, with w_s = exp(E - cum_s) dt'_s: the hi part bf16(w x) into
         // the Xw buffer once block k-1's lo MMA has read it, then the lo part
-        // bf16(w x - hi) once the hi MMA has.  Compact loops: the hot code of all
-        // roles together has to stay within the SM's instruction cache.
+        // bf16(w x - hi) once the hi MMA has.  After each part one thread of warp
+        // 4 issues that part's state MMA (hs += B^T Xw), once the state warps have
+        // read hs for this block.  The four warps meet at a named barrier that
+        // also ANDs their status, so they always leave the loop together.  Compact
+        // loops: the hot code of all roles has to stay in the SM's instruction cache.
         const int q = warp - 4;
         const int t = q * 32 + lane;
         Walker wk;
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
-        while (ok && wk.next(p, c, false)) {
+        while (wk.next(p, c, false)) {
             const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
             const uint32_t tX = 3 * kc + 2;
             const uint8_t *xt = sm.slot[tX % kSlots];
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status) &&
-                       warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status)))
-                break;
+            ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status) &&
+                 warp_wait(sm, &sm.full[tX % kSlots], (tX / kSlots) & 1, status);
             const float w0 = (t < c.l) ? __expf(ar.E[0] - ar.cum[0][t]) * ar.dtp[0][t] : 0.f;
             const float w1 = (t < c.l) ? __expf(ar.E[1] - ar.cum[1][t]) * ar.dtp[1][t] : 0.f;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.arr_free[ab]);
+            if (ok && lane == 0) mbar_arrive(&sm.arr_free[ab]);
             // ---- hi part bf16(w x) into the buffer once block k-1's lo MMA has read it ----
-            if (kc > 0 && !(ok = warp_wait(sm, &sm.xbuf_free, 1, status))) break;
+            ok = ok && (kc == 0 || warp_wait(sm, &sm.xbuf_free, 1, status));
+            if (ok) {
 #pragma unroll 1
             for (int i = 0; i < 16; ++i) {
                 const int hh = i >> 3, cc = i & 7;
@@ -749,11 +734,27 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 o.w = pack2(__fmul2_rn(ww, make_float2(bf16_lo(xv.w), bf16_hi(xv.w))));
                 *reinterpret_cast<uint4 *>(sm.xw[0] + off) = o;
             }
+            }
             fence_proxy_async_smem();
+            if (!xw_group_and(ok)) break;                       // hi part of all four warps in
+            bool issued = true;
+            if (warp == 4 && lane == 0) {
+                const uint32_t tB = 3 * kc + 1;
+                issued = wait_bar(sm, &sm.full[tB % kSlots], (tB / kSlots) & 1, status) &&
+                         wait_bar(sm, &sm.state_ok, kc & 1, status);
+                if (issued) {
+                    tc_fence_after();
+                    const uint64_t db = smem_desc_sw128(smem_u32(sm.slot[tB % kSlots]), kHalfBytes, 1024);
+                    const uint64_t dw = smem_desc_sw128(smem_u32(sm.xw[0]), kHalfBytes, 1024);
+#pragma unroll 1
+                    for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
+                    mma_commit(&sm.xbuf_free);
+                }
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.xhi_ready);
             // ---- lo part bf16(w x - hi) once the hi MMA has read the buffer ----
-            if (!(ok = warp_wait(sm, &sm.xbuf_free, 0, status))) break;
+            ok = warp_wait(sm, &sm.xbuf_free, 0, status);      // fails through the abort flag if not issued
+            if (ok) {
 #pragma unroll 1
             for (int i = 0; i < 16; ++i) {
                 const int hh = i >> 3, cc = i & 7;
@@ -770,10 +771,27 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 }
                 *reinterpret_cast<uint4 *>(sm.xw[0] + off) = make_uint4(o[0], o[1], o[2], o[3]);
             }
+            }
             fence_proxy_async_smem();
+            if (!xw_group_and(ok)) break;                       // lo part of all four warps in
+            if (warp == 4 && lane == 0) {
+                const uint32_t tB = 3 * kc + 1;
+                tc_fence_after();
+                const uint64_t db = smem_desc_sw128(smem_u32(sm.slot[tB % kSlots]), kHalfBytes, 1024);
+                const uint64_t dw = smem_desc_sw128(smem_u32(sm.xw[0]), kHalfBytes, 1024);
+#pragma unroll 1
+                for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
+                mma_commit(&sm.state_done);
+                mma_commit(&sm.xbuf_free);
+                mma_commit(&sm.empty[tB % kSlots]);
+                mma_commit(&sm.empty[tX % kSlots]);          // the Xw passes have read X
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.xlo_ready);
             ++kc;
+        }
+        if (warp == 4 && lane == 0) {                          // the state MMAs' issuing thread
+            mma_commit(&sm.drain_h);
+            wait_bar(sm, &sm.drain_h, 0, nullptr);
         }
     } else if (warp >= 8 && warp < 12) {
         // ===================== S and row scaling (lane = token) =====================
