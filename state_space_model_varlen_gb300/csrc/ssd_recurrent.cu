@@ -96,7 +96,9 @@ __device__ __forceinline__ float softplus_f(float z) {
     return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
 }
 
-template <typename IoT, typename StT, int NPL>
+// kDepth: tokens of input prefetched ahead of the recurrence (a register ring;
+// deeper for narrow states, where registers are cheap and the chain is short).
+template <typename IoT, typename StT, int NPL, int kDepth>
 __global__ void __launch_bounds__(kWarps * 32)
 recurrent_scan_kernel(ScanArgs a, bool vec) {
     const int lane = threadIdx.x & 31;
@@ -159,45 +161,112 @@ recurrent_scan_kernel(ScanArgs a, bool vec) {
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const float Dh = a.D ? a.D[h] : 0.f;
 
-    for (int64_t t = t0; t < t1; ++t) {
-        const float z = a.dt[t * a.H + h] + bias;
-        const float d = a.dt_softplus ? softplus_f(z) : z;
-        const float decay = expf(d * Ah);
-        float xv[kRowsPerWarp], bv[NPL], cv[NPL];
-        const int64_t xrow = (t * a.H + h) * a.P + p0;
-        load_n<IoT, kRowsPerWarp>(X + xrow, xv, a.P - p0, vec);
-        const int64_t brow = (t * a.G + g) * a.N;
-        load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
-        load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
-        float part[kRowsPerWarp];
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const float dx = d * xv[i];
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < NPL; ++j) {
-                st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
-                acc = fmaf(cv[j], st[i][j], acc);
+    if constexpr (kDepth > 1) {
+        // Token inputs (dt, x, B, C) do not depend on the state: they are loaded
+        // kDepth tokens ahead into a register ring, so the sequential chain waits
+        // on arithmetic, not on memory latency.
+        float rd[kDepth], rx[kDepth][kRowsPerWarp], rb[kDepth][NPL], rc[kDepth][NPL];
+        auto fetch = [&](int u, int64_t t) {
+            if (t < t1) {
+                rd[u] = a.dt[t * a.H + h];
+                load_n<IoT, kRowsPerWarp>(X + (t * a.H + h) * a.P + p0, rx[u], a.P - p0, vec);
+                const int64_t brow = (t * a.G + g) * a.N;
+                load_n<IoT, NPL>(Bm + brow + n0, rb[u], nvalid, vec);
+                load_n<IoT, NPL>(Cm + brow + n0, rc[u], nvalid, vec);
             }
-            part[i] = acc;
+        };
+    #pragma unroll
+        for (int u = 0; u < kDepth; ++u) fetch(u, t0 + u);
+
+        for (int64_t tb = t0; tb < t1; tb += kDepth) {
+    #pragma unroll
+            for (int u = 0; u < kDepth; ++u) {
+                const int64_t t = tb + u;
+                if (t >= t1) break;
+                const float z = rd[u] + bias;
+                const float d = a.dt_softplus ? softplus_f(z) : z;
+                const float decay = expf(d * Ah);
+                float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+    #pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = rx[u][i];
+    #pragma unroll
+                for (int j = 0; j < NPL; ++j) { bv[j] = rb[u][j]; cv[j] = rc[u][j]; }
+                fetch(u, t + kDepth);                    // refill this slot with token t + kDepth
+                const int64_t xrow = (t * a.H + h) * a.P + p0;
+                float part[kRowsPerWarp];
+    #pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i) {
+                    const float dx = d * xv[i];
+                    float acc = 0.f;
+    #pragma unroll
+                    for (int j = 0; j < NPL; ++j) {
+                        st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+                        acc = fmaf(cv[j], st[i][j], acc);
+                    }
+                    part[i] = acc;
+                }
+    #pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i)
+    #pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
+                if (lane < kRowsPerWarp && row_ok[lane]) {
+                    float yv = 0.f;
+    #pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i)
+                        if (i == lane) yv = part[i] + Dh * xv[i];
+                    Y[xrow + lane] = from_f<IoT>(yv);
+                }
+                if (inter) {
+                    const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
+    #pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i)
+                        if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+                }
+            }
         }
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i)
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-        if (lane < kRowsPerWarp && row_ok[lane]) {
-            float yv = 0.f;
-#pragma unroll
+    } else {
+        // wide states: registers are scarce, plain loop (occupancy hides latency)
+        for (int64_t t = t0; t < t1; ++t) {
+            const float z = a.dt[t * a.H + h] + bias;
+            const float d = a.dt_softplus ? softplus_f(z) : z;
+            const float decay = expf(d * Ah);
+            float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+            const int64_t xrow = (t * a.H + h) * a.P + p0;
+            load_n<IoT, kRowsPerWarp>(X + xrow, xv, a.P - p0, vec);
+            const int64_t brow = (t * a.G + g) * a.N;
+            load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
+            load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
+            float part[kRowsPerWarp];
+    #pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const float dx = d * xv[i];
+                float acc = 0.f;
+    #pragma unroll
+                for (int j = 0; j < NPL; ++j) {
+                    st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+                    acc = fmaf(cv[j], st[i][j], acc);
+                }
+                part[i] = acc;
+            }
+    #pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i)
-                if (i == lane) yv = part[i] + Dh * xv[i];
-            Y[xrow + lane] = from_f<IoT>(yv);
-        }
-        if (inter) {
-            const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i)
-                if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+    #pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
+            if (lane < kRowsPerWarp && row_ok[lane]) {
+                float yv = 0.f;
+    #pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i)
+                    if (i == lane) yv = part[i] + Dh * xv[i];
+                Y[xrow + lane] = from_f<IoT>(yv);
+            }
+            if (inter) {
+                const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
+    #pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i)
+                    if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+            }
         }
     }
 
@@ -213,11 +282,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <typename IoT, typename StT, int NPL>
 cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t stream) {
+    constexpr int kDepth = NPL <= 2 ? 4 : 1;
     // vector accesses need every row start aligned to the vector width
     const bool vec = (a.N % NPL == 0) && (a.P % kRowsPerWarp == 0) && aligned16(a.x) &&
                      aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
                      aligned16(a.out_intermediate);
-    recurrent_scan_kernel<IoT, StT, NPL><<<grid, block, 0, stream>>>(a, vec);
+    recurrent_scan_kernel<IoT, StT, NPL, kDepth><<<grid, block, 0, stream>>>(a, vec);
     return cudaGetLastError();
 }
 
