@@ -175,53 +175,62 @@ recurrent_scan_kernel(ScanArgs a, bool vec) {
                 load_n<IoT, NPL>(Cm + brow + n0, rc[u], nvalid, vec);
             }
         };
-    #pragma unroll
+#pragma unroll
         for (int u = 0; u < kDepth; ++u) fetch(u, t0 + u);
 
         for (int64_t tb = t0; tb < t1; tb += kDepth) {
-    #pragma unroll
+            // the group's dt activations, decays and inputs, then the refill; only
+            // the state update below is sequential, the rest is independent work
+            float dd[kDepth], dec[kDepth], xs[kDepth][kRowsPerWarp], bs[kDepth][NPL], cs[kDepth][NPL];
+#pragma unroll
             for (int u = 0; u < kDepth; ++u) {
-                const int64_t t = tb + u;
-                if (t >= t1) break;
                 const float z = rd[u] + bias;
-                const float d = a.dt_softplus ? softplus_f(z) : z;
-                const float decay = expf(d * Ah);
-                float xv[kRowsPerWarp], bv[NPL], cv[NPL];
-    #pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = rx[u][i];
-    #pragma unroll
-                for (int j = 0; j < NPL; ++j) { bv[j] = rb[u][j]; cv[j] = rc[u][j]; }
-                fetch(u, t + kDepth);                    // refill this slot with token t + kDepth
-                const int64_t xrow = (t * a.H + h) * a.P + p0;
-                float part[kRowsPerWarp];
-    #pragma unroll
+                dd[u] = a.dt_softplus ? softplus_f(z) : z;
+                dec[u] = expf(dd[u] * Ah);
+#pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i) xs[u][i] = rx[u][i];
+#pragma unroll
+                for (int j = 0; j < NPL; ++j) { bs[u][j] = rb[u][j]; cs[u][j] = rc[u][j]; }
+            }
+#pragma unroll
+            for (int u = 0; u < kDepth; ++u) fetch(u, tb + kDepth + u);   // tokens of the next group
+            float part[kDepth][kRowsPerWarp];
+#pragma unroll
+            for (int u = 0; u < kDepth; ++u) {
+                const bool live = tb + u < t1;
+#pragma unroll
                 for (int i = 0; i < kRowsPerWarp; ++i) {
-                    const float dx = d * xv[i];
+                    const float dx = dd[u] * xs[u][i];
                     float acc = 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < NPL; ++j) {
-                        st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
-                        acc = fmaf(cv[j], st[i][j], acc);
+                        if (live) st[i][j] = fmaf(dec[u], st[i][j], dx * bs[u][j]);
+                        acc = fmaf(cs[u][j], st[i][j], acc);
                     }
-                    part[i] = acc;
+                    part[u][i] = acc;
                 }
-    #pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i)
-    #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-                if (lane < kRowsPerWarp && row_ok[lane]) {
-                    float yv = 0.f;
-    #pragma unroll
-                    for (int i = 0; i < kRowsPerWarp; ++i)
-                        if (i == lane) yv = part[i] + Dh * xv[i];
-                    Y[xrow + lane] = from_f<IoT>(yv);
-                }
-                if (inter) {
-                    const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
-    #pragma unroll
+                if (live && inter) {
+                    const int64_t ibase = (((tb + u) * a.H + h) * a.P + p0) * a.N;
+#pragma unroll
                     for (int i = 0; i < kRowsPerWarp; ++i)
                         if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kDepth; ++u)
+#pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i], off);
+#pragma unroll
+            for (int u = 0; u < kDepth; ++u) {
+                if (tb + u < t1 && lane < kRowsPerWarp && row_ok[lane]) {
+                    float yv = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i)
+                        if (i == lane) yv = part[u][i] + Dh * xs[u][i];
+                    Y[((tb + u) * a.H + h) * a.P + p0 + lane] = from_f<IoT>(yv);
                 }
             }
         }
@@ -238,32 +247,32 @@ recurrent_scan_kernel(ScanArgs a, bool vec) {
             load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
             load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
             float part[kRowsPerWarp];
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i) {
                 const float dx = d * xv[i];
                 float acc = 0.f;
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < NPL; ++j) {
                     st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
                     acc = fmaf(cv[j], st[i][j], acc);
                 }
                 part[i] = acc;
             }
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i)
-    #pragma unroll
+#pragma unroll
                 for (int off = 16; off > 0; off >>= 1)
                     part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
             if (lane < kRowsPerWarp && row_ok[lane]) {
                 float yv = 0.f;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < kRowsPerWarp; ++i)
                     if (i == lane) yv = part[i] + Dh * xv[i];
                 Y[xrow + lane] = from_f<IoT>(yv);
             }
             if (inter) {
                 const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < kRowsPerWarp; ++i)
                     if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
             }
