@@ -217,3 +217,28 @@ def test_decay_regimes(regime):
         p.dt = rng.uniform(0.001, 0.1, size=p.dt.shape).astype(np.float32)
         p.A = np.array([-1e-3, -1e-4, -2e-3, 0.0], dtype=np.float32)
     _run_and_check(p)
+
+
+def test_long_single_sequence_keeps_state_accuracy():
+    """One 40,000-token sequence (313 blocks) from an initial state: the final
+    state still meets the fp32-storage tolerance after every block's update, and
+    y agrees at the start, the middle and the end of the sequence."""
+    p = W.make_problem([40000], nheads=2, headdim=64, dstate=128, ngroups=1, num_slots=3,
+                       has_init=[1], cache_std=0.3, seed=51)
+    out = Hn.run_gpu(p)
+    assert out["status"] == 0 and out["path"] == "chunked_tc"
+    ref = oracle.ssd_scan_reference(p)
+    Hn.check_state(out["cache"][p.slot_idx[0]], ref["final"][0], p.state_dtype)
+    for a, b in ((0, 512), (19968, 20480), (39488, 40000)):
+        Hn.check_y(out["y"][a:b], ref["y"][a:b], p.io_dtype)
+
+
+def test_more_sequences_than_the_longest_first_sort_holds():
+    """8,200 short sequences (4 to 9 tokens) on the tensor-core path: more than the
+    prep kernel sorts, so the sequences are dealt in their given order."""
+    rng = np.random.default_rng(52)
+    lens = rng.integers(4, 10, size=8200)
+    p = W.make_problem(lens, nheads=2, headdim=64, dstate=128, ngroups=1, num_slots=8200,
+                       cache_std=0.1, seed=52)
+    out, _ = _run_and_check(p)
+    assert out["path"] == "chunked_tc"
