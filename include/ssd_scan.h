@@ -121,8 +121,11 @@ typedef struct {
 } ssd_scan_params;
 
 /* Bytes of device workspace a call with these parameters needs (a function
- * of S and the selected kernel only; may be 0).  The workspace must be
- * 256-byte aligned and is overwritten by the call.  Returns 0 for invalid
+ * of T, S, H and the selected kernel only; may be 0).  The workspace must be
+ * 256-byte aligned and is overwritten by the call.  On the tensor-core path it
+ * holds the longest-first sequence order and, for batches whose work is spread
+ * over several SMs per sequence, the fp32 states that segments of one sequence
+ * hand to each other (at most 1024 x 64 KiB).  Returns 0 for invalid
  * parameters as well; ssd_scan_varlen reports those. */
 size_t ssd_scan_varlen_workspace_size(const ssd_scan_params *params);
 
@@ -160,6 +163,10 @@ const char *ssd_scan_varlen_path(const ssd_scan_params *params);
  *     (unordered streams) race on it; order them on one stream or use
  *     ssd_scan_varlen with separate workspaces.  Nothing in the array needs
  *     to start zeroed: each call rewrites what it reads.
+ *   - Every sequence runs whole on one CTA (the array has no room for the
+ *     hand-over states), so for batches that ssd_scan_varlen cuts into
+ *     segments the results agree with it within rounding, not bit for bit,
+ *     and take longer.
  * Everything else (arguments, aliasing, errors, results) is as for
  * ssd_scan_varlen. */
 ssd_status ssd_scan_varlen_noalloc(const ssd_scan_params *params, struct CUstream_st *stream);

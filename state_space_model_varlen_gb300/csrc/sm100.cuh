@@ -86,6 +86,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
 }
 
 // Warm L2 with one box of a tiled tensor (no shared-memory destination).
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (ptr 16-byte aligned, bytes a
+// multiple of 16); a hint without effect on the memory model.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),

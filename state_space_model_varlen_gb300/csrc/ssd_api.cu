@@ -40,6 +40,7 @@ ssd::ScanArgs make_args(const ssd_scan_params *p) {
     ssd::ScanArgs a;
     a.T = p->total_tokens;
     a.S = p->num_seqs;
+    a.max_seqlen = p->max_seqlen;
     a.H = p->nheads;
     a.P = p->headdim;
     a.N = p->dstate;
@@ -110,7 +111,7 @@ ssd_status ssd_scan_varlen(const ssd_scan_params *params, struct CUstream_st *st
         if (need > 0 && (params->workspace == nullptr || params->workspace_bytes < need ||
                          (reinterpret_cast<uintptr_t>(params->workspace) & 255u) != 0))
             return SSD_ERR_WORKSPACE;
-        err = ssd::launch_chunked(a, params->state_dtype, params->workspace, stream);
+        err = ssd::launch_chunked(a, params->state_dtype, params->workspace, params->workspace_bytes, stream);
     } else {
         err = ssd::launch_recurrent(a, params->io_dtype, params->state_dtype, stream);
     }

@@ -50,6 +50,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstddef>
 #include <mutex>
 
@@ -75,6 +76,14 @@ constexpr uint64_t kSpinLimit = 4000000000ull;   // clock cycles (~2 s) per wait
 constexpr float kDiagFactorLimit = 80.f;         // |decay| of a 32-token block for the
                                                  // factored diagonal path (e^80 < fp32 max)
 constexpr float kScaleLimit = 80.f;              // |exponent| bound of the scaled state inputs
+// Segments: long items are cut into segments of `seg` blocks dealt to different
+// CTAs, the state handed over in fp32 through the workspace (see prep kernel).
+constexpr int kMaxLevels = 32;                   // segments per item at most
+constexpr int kMetaInts = 64;                    // [0] items, [1] seg, [2] levels, [4 + j] level offsets
+constexpr int kSegMinBlocks = 6;                 // blocks per segment at least
+constexpr int kSegPerSm = 8;                     // segments per SM aimed at
+constexpr int kSegSlots = 1024;                  // handed-over states the workspace holds at most
+constexpr size_t kSegStateBytes = 2 * 64 * 128 * sizeof(float);   // one head pair's fp32 state
 
 // TMEM columns
 constexpr uint32_t kColG = 0;      // G / S (in place), lanes = tokens
@@ -92,6 +101,10 @@ struct Params {
     int32_t dt_softplus, write_final, state_dtype;
     const float *dt, *dt_bias, *A, *D;
     const int32_t *cu_seqlens, *slot_idx, *order;
+    const int32_t *meta, *bstart;                 // segmentation (valid when seg_enabled)
+    int32_t *seg_flags;                           // per boundary, head pair and state warp: published
+    float *seg_state;                             // per boundary and head pair: fp32 h [2][64][128]
+    int32_t seg_enabled;
     const uint8_t *has_init;
     void *state_cache, *out_y;
     const void *x;
@@ -121,6 +134,16 @@ struct __align__(16) Arrays {
     int32_t exact[2][4];   // diagonal block needs the per-element path
 };
 
+// One work item: a segment of a sequence for a pair of heads of one B/C group.
+struct __align__(16) Item {
+    int32_t round;                // deal round after this item
+    int32_t seq, h0, g, slot, t0, len, bin, bout;
+    int32_t flags;                // bit 0: found, 1: initial state, 2: from the workspace,
+                                  // 3: final state to the workspace
+};
+constexpr int kItemRing = 8;      // items looked up ahead by the item warp
+constexpr uint32_t kItemTakers = 15;   // walkers per item: 2 single threads + 13 warps
+
 struct __align__(1024) Smem {
     uint8_t slot[kSlots][kTileBytes];     // TMA ring: C / B [n half][s][n], X [head][s][p]
     uint8_t xw[2][kHalfBytes];            // Xw (hi, then lo), [head][s][p], 128-B swizzle
@@ -132,6 +155,8 @@ struct __align__(1024) Smem {
     uint64_t hs_a, hs_b, hbuf_a_done, state_ok, state_done;
     uint64_t yinter_ready, y_scaled, y_ready[2], y_free[2], x_epi_done[2];
     uint64_t drain_y, drain_h;
+    uint64_t item_full[kItemRing], item_empty[kItemRing];
+    Item items[kItemRing];
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -151,36 +176,45 @@ struct Chunk {
     int32_t seq, h0, g, slot;
     int32_t row0;        // first token of this block (total tokens < 2^31 on this path)
     int32_t l;           // valid tokens in this block
+    int32_t bin, bout;   // workspace state slots read at the first / written at the last block
     bool init, first, last, empty_item;
-};
-
-// One work item: a sequence and a pair of heads of one B/C group.
-struct Item {
-    int32_t round;                // deal round after this item
-    int32_t seq, h0, g, slot, t0, len;
-    int32_t flags;                // bit 0: found, bit 1: has an initial state
+    bool init_ws;        // the initial state comes from the workspace (a previous segment)
+    bool fin_ws;         // the final state goes to the workspace (a following segment)
 };
 
 // Next valid item of this CTA (longest sequences first, snake order over the
-// CTAs), starting at deal round `round`.  Out of line: called once per item.
+// CTAs), starting at deal round `round`.  With segmentation the items are
+// dealt level by level -- every item's first segment, then every second
+// segment, ... -- so a segment's predecessor is always dealt earlier; the
+// sequences with a j-th segment are a prefix of the longest-first order.
+// Out of line: called once per item.
 __device__ __noinline__ Item find_item(const Params &p, int32_t round, bool report) {
     Item it;
     it.flags = 0;
     const int32_t hp_per_seq = p.H / 2;
     const int32_t grid = gridDim.x, cta = blockIdx.x;
+    const int32_t num_items = p.seg_enabled ? p.meta[0] : p.num_items;
+    const int32_t seg = p.seg_enabled ? p.meta[1] : 0x40000000;
+    const int32_t nlev = p.seg_enabled ? p.meta[2] : 1;
     while (true) {
         const int32_t base = round * grid;
         const int32_t idx = base + ((round & 1) ? (grid - 1 - cta) : cta);
         ++round;
-        if (base >= p.num_items) break;
-        if (idx >= p.num_items) continue;
-        const int32_t rank = idx / hp_per_seq;
-        const int32_t hp = idx - rank * hp_per_seq;
+        if (base >= num_items) break;
+        if (idx >= num_items) continue;
+        int32_t j = 0, off = 0;
+        if (p.seg_enabled) {
+            while (j + 1 < nlev && idx >= p.meta[4 + j + 1]) ++j;
+            off = p.meta[4 + j];
+        }
+        const int32_t r = idx - off;
+        const int32_t rank = r / hp_per_seq;
+        const int32_t hp = r - rank * hp_per_seq;
         const int32_t seq = p.order[rank];
         const int32_t h0 = hp * 2;
         const int64_t a = p.cu_seqlens[seq], e = p.cu_seqlens[seq + 1];
         if (a < 0 || e < a || e > p.T) {
-            if (report && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SEQLENS);
+            if (report && j == 0 && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SEQLENS);
             continue;
         }
         const bool init = p.has_init != nullptr && p.has_init[seq] != 0;
@@ -188,60 +222,29 @@ __device__ __noinline__ Item find_item(const Params &p, int32_t round, bool repo
         if (init || p.write_final) {
             slot = p.slot_idx[seq];
             if (slot < 0 || slot >= p.num_slots) {
-                if (report && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SLOT);
+                if (report && j == 0 && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SLOT);
                 continue;
             }
         }
+        const int32_t len = (int32_t)(e - a);
+        const int32_t nb = (len + kQ - 1) / kQ;
+        const int32_t nseg = nb == 0 ? 1 : (nb + seg - 1) / seg;
+        const int32_t b0 = j * seg, b1 = min(nb, (j + 1) * seg);
         it.seq = seq;
         it.h0 = h0;
         it.g = h0 / p.hpg;
         it.slot = slot;
-        it.t0 = (int32_t)a;
-        it.len = (int32_t)(e - a);
-        it.flags = 1 | (init ? 2 : 0);
+        it.t0 = (int32_t)a + b0 * kQ;
+        it.len = nb == 0 ? 0 : min(len, b1 * kQ) - b0 * kQ;
+        it.bin = j > 0 ? (p.bstart[rank] + j - 1) * hp_per_seq + hp : 0;
+        it.bout = j + 1 < nseg ? (p.bstart[rank] + j) * hp_per_seq + hp : 0;
+        it.flags = 1 | ((j > 0 || init) ? 2 : 0) | (j > 0 ? 4 : 0) | (j + 1 < nseg ? 8 : 0);
         break;
     }
     it.round = round;
     return it;
 }
 
-// Walks this CTA's items block by block; identical in every role.
-struct Walker {
-    Item it;
-    int32_t nb = 0, b = 0;
-    bool have = false;
-
-    __device__ Walker() { it.round = 0; }
-
-    // Next event: a block of an item, or (if want_empty) an item without tokens.
-    __device__ bool next(const Params &p, Chunk &c, bool want_empty, bool report = false) {
-        while (true) {
-            if (!have || b >= nb) {
-                it = find_item(p, it.round, report);
-                if (!(it.flags & 1)) return false;
-                have = true;
-                nb = (it.len + kQ - 1) / kQ;
-                b = 0;
-                if (nb == 0) {
-                    if (want_empty) {
-                        c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot; c.row0 = it.t0; c.l = 0;
-                        c.init = (it.flags & 2) != 0; c.first = c.last = true; c.empty_item = true;
-                        return true;
-                    }
-                    continue;
-                }
-            }
-            c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot; c.init = (it.flags & 2) != 0;
-            c.row0 = it.t0 + b * kQ;
-            c.l = min(kQ, it.len - b * kQ);
-            c.first = (b == 0);
-            c.last = (b == nb - 1);
-            c.empty_item = false;
-            ++b;
-            return true;
-        }
-    }
-};
 
 // ---------------------------------------------------------------------------
 // bounded waits
@@ -298,6 +301,109 @@ __device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t pari
     return __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) || warp_wait_slow(sm, bar, parity, status);
 }
 
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *f) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t *f, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+// Whole-warp wait until another CTA has published a segment's final state
+// (every lane acquires the flag itself).  Bounded like the barrier waits.
+__device__ __noinline__ bool warp_wait_flag(Smem &sm, const int32_t *flag, int32_t *status) {
+    const uint64_t t_start = clock64();
+    uint32_t it = 0;
+    while (!__all_sync(0xffffffffu, ld_acquire_gpu(flag) != 0)) {
+        if ((++it & 63u) == 0) {
+            int give_up = 0;
+            if ((threadIdx.x & 31) == 0) {
+                if (*(volatile int32_t *)&sm.abort_flag) {
+                    give_up = 1;
+                } else if (clock64() - t_start > kSpinLimit) {
+                    atomicExch(&sm.abort_flag, 1);
+                    if (status) atomicOr(status, SSD_DEV_TIMEOUT);
+                    give_up = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
+// The ik-th item of this CTA from the ring (flags 0: no more items, or the
+// wait gave up).  Out of line: called once per item in every role.
+__device__ __noinline__ Item take_item(Smem &sm, uint32_t ik, bool whole_warp, int32_t *status) {
+    const uint32_t s = ik % kItemRing, par = (ik / kItemRing) & 1;
+    Item it;
+    if (!(whole_warp ? warp_wait(sm, &sm.item_full[s], par, status)
+                     : wait_bar(sm, &sm.item_full[s], par, status))) {
+        it.flags = 0;
+        return it;
+    }
+    it = sm.items[s];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(&sm.item_empty[s]);
+    return it;
+}
+
+// Walks this CTA's items block by block; identical in every role.  The items
+// come from a ring in shared memory that the item warp fills ahead of use,
+// so no role waits on the lookups' global loads at an item boundary.
+// whole_warp: all 32 lanes of a warp walk together (else one thread alone).
+struct Walker {
+    Item it;
+    int32_t nb = 0, b = 0;
+    uint32_t ik = 0;              // items taken from the ring
+    bool have = false;
+
+    __device__ void fill(Chunk &c) const {
+        c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot;
+        c.init = (it.flags & 2) != 0;
+        c.init_ws = (it.flags & 4) != 0;
+        c.fin_ws = (it.flags & 8) != 0;
+        c.bin = it.bin;
+        c.bout = it.bout;
+    }
+
+    __device__ bool take(Smem &sm, bool whole_warp, int32_t *status) {
+        it = take_item(sm, ik++, whole_warp, status);
+        return (it.flags & 1) != 0;
+    }
+
+    // Next event: a block of an item, or (if want_empty) an item without tokens.
+    __device__ bool next(Smem &sm, Chunk &c, bool want_empty, bool whole_warp, int32_t *status) {
+        while (true) {
+            if (!have || b >= nb) {
+                if (!take(sm, whole_warp, status)) return false;
+                have = true;
+                nb = (it.len + kQ - 1) / kQ;
+                b = 0;
+                if (nb == 0) {
+                    if (want_empty) {
+                        fill(c);
+                        c.row0 = it.t0; c.l = 0;
+                        c.first = c.last = true; c.empty_item = true;
+                        return true;
+                    }
+                    continue;
+                }
+            }
+            fill(c);
+            c.row0 = it.t0 + b * kQ;
+            c.l = min(kQ, it.len - b * kQ);
+            c.first = (b == 0);
+            c.last = (b == nb - 1);
+            c.empty_item = false;
+            ++b;
+            return true;
+        }
+    }
+};
+
 // Barrier over the four Xw warps (named barrier 1) that also ANDs a flag over
 // them, so that the group takes every exit together.
 __device__ __forceinline__ bool xw_group_and(bool v) {
@@ -342,10 +448,28 @@ template <> __device__ __forceinline__ void store_state<__half>(__half *p, float
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 1024;
 constexpr int kSortMax = 8192;
+constexpr int kPrepSmem = 2 * kSortMax * (int)sizeof(int32_t);   // dynamic shared memory of the prep kernel
 
+// Longest-first order of the sequences (by block count), and, when enabled,
+// their cut into segments: seg blocks per segment, chosen so that about
+// kSegPerSm segments fall to each SM when the longest item is shorter than an
+// SM's mean share of the blocks (long equal items otherwise leave most SMs idle
+// in the last deal round); at most kMaxLevels segments per item, at least
+// kSegMinBlocks blocks per segment and at most `cap` handed-over states
+// (boundaries x head pairs, the workspace's capacity).  Writes order[S], and
+// with segmentation meta
+// (item count, seg, levels, level offsets), bstart[rank] (first boundary of
+// each sequence) and clears the boundary flags of this call.
 __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t *cu, int S, int64_t T,
-                                                                    int32_t *order) {
-    __shared__ int32_t nb[kSortMax];
+                                                                    int32_t *order, int32_t *meta,
+                                                                    int32_t *bstart, int32_t *flags, int hp,
+                                                                    int num_sms, int cap, int seg_enabled) {
+    extern __shared__ int32_t prep_smem[];
+    int32_t *nb = prep_smem;                     // block count by sequence
+    int32_t *nbr = prep_smem + kSortMax;         // block count by rank
+    __shared__ int32_t part[kPrepThreads / 32];
+    __shared__ uint32_t total;                   // blocks of all sequences (< 2^25 here)
+    __shared__ int32_t seg_s;
     if (S > kSortMax) {
         for (int s = threadIdx.x; s < S; s += blockDim.x) order[s] = s;
         return;
@@ -354,7 +478,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
         const int64_t a = cu[s], e = cu[s + 1];
         nb[s] = (a < 0 || e < a || e > T) ? 0 : (int32_t)((e - a + kQ - 1) / kQ);
     }
+    if (threadIdx.x == 0) total = 0;
     __syncthreads();
+    uint32_t mine = 0;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int32_t v = nb[s];
         int rank = 0;
@@ -363,6 +489,84 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
             rank += (u > v) || (u == v && q < s);
         }
         order[rank] = s;
+        nbr[rank] = v;
+        mine += v;
+    }
+    if (!seg_enabled) return;
+    mine = __reduce_add_sync(0xffffffffu, mine);
+    if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&total, mine);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const long long work = (long long)total * hp;
+        int seg = 0x40000000;
+        // Only when the longest item is shorter than an SM's mean share: a
+        // longer one is the critical path already, and its segments would run
+        // one after another anyway.
+        if (cap > 0 && (long long)nbr[0] * num_sms < work) {
+            // boundaries x hp <= total x hp / seg <= cap
+            long long v = max((long long)kSegMinBlocks, (work + (long long)kSegPerSm * num_sms - 1) / ((long long)kSegPerSm * num_sms));
+            v = max(v, (work + cap - 1) / cap);
+            v = max(v, (long long)(nbr[0] + kMaxLevels - 1) / kMaxLevels);
+            seg = (int)min(v, 0x40000000LL);
+        }
+        seg_s = seg;
+    }
+    __syncthreads();
+    const int seg = seg_s;
+    // boundaries per rank: nseg - 1; exclusive prefix sum into bstart
+    constexpr int kPer = kSortMax / kPrepThreads;
+    const int r0 = threadIdx.x * kPer;
+    int32_t local = 0;
+    for (int k = 0; k < kPer; ++k) {
+        const int r = r0 + k;
+        if (r < S) local += nbr[r] == 0 ? 0 : (nbr[r] + seg - 1) / seg - 1;
+    }
+    // block-wide exclusive scan of `local`
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int32_t incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) part[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int32_t v = part[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        part[lane] = v;                          // inclusive over warps
+    }
+    __syncthreads();
+    int32_t run = (w ? part[w - 1] : 0) + incl - local;
+    for (int k = 0; k < kPer; ++k) {
+        const int r = r0 + k;
+        if (r < S) {
+            bstart[r] = run;
+            run += nbr[r] == 0 ? 0 : (nbr[r] + seg - 1) / seg - 1;
+        }
+    }
+    const int32_t nbound = part[31];
+    for (int i = threadIdx.x; i < nbound * hp * 4; i += blockDim.x) flags[i] = 0;
+    if (threadIdx.x == 0) {
+        const int nlev = nbr[0] == 0 ? 1 : (nbr[0] + seg - 1) / seg;
+        // sequences with a j-th segment are the first cnt_j ranks (block counts are sorted)
+        int32_t offs = 0;
+        for (int j = 0; j < nlev; ++j) {
+            meta[4 + j] = offs;
+            int lo = 0, hi = S;                  // first rank whose item has no j-th segment
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const int ns = nbr[mid] == 0 ? 1 : (nbr[mid] + seg - 1) / seg;
+                if (ns > j) lo = mid + 1; else hi = mid;
+            }
+            offs += lo * hp;
+        }
+        meta[4 + nlev] = offs;
+        meta[0] = offs;
+        meta[1] = seg;
+        meta[2] = nlev;
     }
 }
 
@@ -541,6 +745,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         mbar_init(&sm.y_scaled, 4);
         mbar_init(&sm.drain_y, 1);
         mbar_init(&sm.drain_h, 1);
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(&sm.item_full[i], 1);
+            mbar_init(&sm.item_empty[i], kItemTakers);
+        }
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -565,7 +773,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             Chunk c;
             uint32_t kc = 0, issued = 0;
             bool ok = true;
-            while (ok && wk.next(p, c, false, true)) {
+            while (ok && wk.next(sm, c, false, false, status)) {
                 const int32_t row = c.row0;
 #pragma unroll 1
                 for (int j = 0; j < 3; ++j) {                    // C, B, X
@@ -603,7 +811,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             uint32_t kc = 0;
             bool ok = true;
             const uint32_t bH = smem_u32(sm.hbuf);
-            while (ok && wk.next(p, c, false)) {
+            while (ok && wk.next(sm, c, false, false, status)) {
                 const uint32_t tC = 3 * kc, tB = 3 * kc + 1, tX = 3 * kc + 2;
                 const uint32_t bC = smem_u32(sm.slot[tC % kSlots]);
                 const uint32_t bB = smem_u32(sm.slot[tB % kSlots]);
@@ -671,7 +879,24 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             wait_bar(sm, &sm.drain_y, 0, nullptr);
         }
     } else if (warp == 3) {
-        // no role: the state MMAs are issued from the Xw warps
+        // ===================== item dealer =====================
+        // Looks this CTA's items up in deal order (one thread) and hands them to
+        // the walkers of every role through the ring, up to kItemRing ahead;
+        // the last entry is the end marker.
+        if (lane == 0) {
+            int32_t round = 0;
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t s = k % kItemRing;
+                if (k >= (uint32_t)kItemRing &&
+                    !wait_bar(sm, &sm.item_empty[s], ((k / kItemRing) - 1) & 1, status))
+                    break;
+                const Item it = find_item(p, round, true);
+                round = it.round;
+                sm.items[s] = it;
+                mbar_arrive(&sm.item_full[s]);
+                if (!(it.flags & 1)) break;
+            }
+        }
       } else {
         // ===================== dt warp (also owns the TMEM allocation) =====================
         Walker wk;
@@ -680,10 +905,21 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         DtOut ds;
         ds.R0 = ds.R1 = 0.f;
         ds.ok = 1;
-        bool have = wk.next(p, c, false);
+        // An item's initial state into L2 a few blocks before the state warps load it.
+        auto prefetch_init = [&](const Chunk &x) {
+            if (!(x.first && x.init) || lane != 0) return;
+            if (x.init_ws)
+                bulk_prefetch_l2(p.seg_state + (size_t)x.bin * (2 * kP * kN), 2 * kP * kN * sizeof(float));
+            else
+                bulk_prefetch_l2(static_cast<const StT *>(p.state_cache) + ((int64_t)x.slot * p.H + x.h0) * (kP * kN),
+                                 2 * kP * kN * sizeof(StT));
+        };
+        bool have = wk.next(sm, c, false, true, status);
+        if (have) prefetch_init(c);
         DtRaw dr = have ? dt_load(p, c.row0, c.l, c.h0) : DtRaw{};
         while (ds.ok && have) {
-            const bool have_n = wk.next(p, cn, false);
+            const bool have_n = wk.next(sm, cn, false, true, status);
+            if (have_n) prefetch_init(cn);
             const DtRaw drn = have_n ? dt_load(p, cn.row0, cn.l, cn.h0) : DtRaw{};   // next block's dt, early
             ds = dt_prep(sm, p, dr, c.l, c.h0, c.first, k, ds.R0, ds.R1, status);
             ++k;
@@ -707,7 +943,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
-        while (wk.next(p, c, false)) {
+        while (wk.next(sm, c, false, true, status)) {
             const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
             const uint32_t tX = 3 * kc + 2;
@@ -802,7 +1038,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         Chunk c;
         uint32_t kc = 0;
         bool ok = true;
-        while (ok && wk.next(p, c, false)) {
+        while (ok && wk.next(sm, c, false, true, status)) {
             const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
             const uint32_t ycol = kColY + 128 * (kc & 1);
@@ -914,6 +1150,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         Walker wk;
         Chunk c;
         uint32_t kc = 0;
+        int32_t pend = 0;                 // 1 + state slot stored but not yet published
+        // Each warp publishes its own 32 rows n of a handed-over state (the rows
+        // the same warp of the next segment's CTA reads): fence, then the flag.
+        auto publish = [&]() {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(p.seg_flags + (size_t)(pend - 1) * 4 + q, 1);
+            pend = 0;
+        };
         bool ok = true;
         StT *cache = static_cast<StT *>(p.state_cache);
         int32_t prev_row0 = 0, prev_l = 0, prev_h0 = 0;   // previous block, for its y epilogue
@@ -963,7 +1208,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (lane == 0) mbar_arrive(&sm.x_epi_done[k & 1]);
             return true;
         };
-        while (ok && wk.next(p, c, true)) {
+        while (ok && wk.next(sm, c, true, true, status)) {
             const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
             if (c.empty_item) {
                 if (p.write_final) {
@@ -980,15 +1225,43 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (!c.first) {
                 if (!(ok = warp_wait(sm, &sm.state_done, (kc - 1) & 1, status))) break;
                 tc_fence_after();
-            } else {
-                // the item's initial state (or zeros) into the accumulator columns
+            } else if (!c.init) {
 #pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 8; ++j) {             // zeros into the accumulator columns
                     uint32_t r[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        r[i] = __float_as_uint(c.init ? load_state<StT>(cache + hbase + (int64_t)(j * 16 + i) * kN) : 0.f);
+                    for (int i = 0; i < 16; ++i) r[i] = 0u;
                     tmem_st16(tmem + lane_off + kColH + 16 * j, r);
+                }
+                tmem_wait_st();
+            } else {
+                // the item's initial state into the accumulator columns: the state
+                // the previous segment's CTA handed over (possibly this CTA, its
+                // publication still pending), else the cache; 64 loads in flight
+                const float *ws = nullptr;
+                if (c.init_ws) {
+                    // publish a pending state first if this has to wait: the CTA
+                    // that is to set the flag may be waiting for that one
+                    const int32_t *fl = p.seg_flags + (size_t)c.bin * 4 + q;
+                    if (!__all_sync(0xffffffffu, ld_acquire_gpu(fl) != 0)) {
+                        if (pend) publish();
+                        if (!(ok = warp_wait_flag(sm, fl, status))) break;
+                    }
+                    ws = p.seg_state + (size_t)c.bin * (2 * kP * kN) + n;
+                }
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t r[64];
+                    if (ws) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__ldcg(ws + (j * 64 + i) * kN));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            r[i] = __float_as_uint(load_state<StT>(cache + hbase + (int64_t)(j * 64 + i) * kN));
+                    }
+                    tmem_st32(tmem + lane_off + kColH + 64 * j, *reinterpret_cast<const uint32_t(*)[32]>(r));
+                    tmem_st32(tmem + lane_off + kColH + 64 * j + 32, *reinterpret_cast<const uint32_t(*)[32]>(r + 32));
                 }
                 tmem_wait_st();
             }
@@ -1054,6 +1327,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(first_half ? &sm.hs_a : &sm.hs_b);
+            if (pend) publish();
             // ---- y of the previous block ----
             if (kc > 0 && !(ok = epilogue(kc - 1))) break;
             prev_row0 = c.row0;
@@ -1063,7 +1337,24 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 // final state of the item: h = hs * exp(R after the block)
                 if (!(ok = warp_wait(sm, &sm.state_done, kc & 1, status))) break;
                 tc_fence_after();
-                if (p.write_final) {
+                if (c.fin_ws) {
+                    // hand the state to the next segment: fp32 h, then the flag
+                    float *ws = p.seg_state + (size_t)c.bout * (2 * kP * kN) + n;
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_off + kColH + 32 * j, r);
+                        tmem_wait_ld();
+                        const float2 ef = (j >> 1) ? ef1 : ef0;
+#pragma unroll
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ef);
+                            __stcg(ws + (j * 32 + 2 * i2) * kN, h.x);
+                            __stcg(ws + (j * 32 + 2 * i2 + 1) * kN, h.y);
+                        }
+                    }
+                    pend = c.bout + 1;            // published once the next block's h copy is out
+                } else if (p.write_final) {
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
                         uint32_t r[32];
@@ -1082,6 +1373,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             }
             ++kc;
         }
+        if (pend) publish();
         if (ok && kc > 0) epilogue(kc - 1);       // y of the last block
     }
 
@@ -1131,14 +1423,44 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows) {
 struct DeviceInfo {
     int sms = 0;
     bool attr_set[3] = {false, false, false};
+    bool prep_attr_set = false;
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
+
+// Workspace: the longest-first order, then (segmentation) the level table,
+// each rank's first boundary, four flags (one per state warp) and one fp32
+// state per handed-over state.  `cap` states at most: no more than kSegSlots, and no more than the
+// batch can have with kSegMinBlocks-block segments.
+struct WsLayout {
+    size_t meta = 0, bstart = 0, flags = 0, states = 0, total = 0;
+    int32_t cap = 0;
+};
+
+size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int64_t T, int32_t S, int32_t H) {
+    WsLayout L;
+    L.total = round256((size_t)S * sizeof(int32_t));
+    if (S <= 0 || S > kSortMax) return L;
+    const int64_t blocks = (T + kQ - 1) / kQ + S;       // >= sum over sequences of their block counts
+    const int64_t cap = std::min<int64_t>(kSegSlots, blocks * (H / 2) / kSegMinBlocks);
+    if (cap <= 0) return L;
+    L.cap = (int32_t)cap;
+    L.meta = L.total;
+    L.bstart = L.meta + round256(kMetaInts * sizeof(int32_t));
+    L.flags = L.bstart + round256((size_t)S * sizeof(int32_t));
+    L.states = L.flags + round256((size_t)cap * 4 * sizeof(int32_t));
+    L.total = L.states + (size_t)cap * kSegStateBytes;
+    return L;
+}
 
 template <typename StT>
-cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStream_t stream) {
+cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1157,6 +1479,11 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStr
             if (e != cudaSuccess) return e;
             di.attr_set[st_idx] = true;
         }
+        if (!di.prep_attr_set) {
+            e = cudaFuncSetAttribute(prep_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+            if (e != cudaSuccess) return e;
+            di.prep_attr_set = true;
+        }
         sms = di.sms;
     }
     CUtensorMap mx, mb, mc;
@@ -1164,8 +1491,30 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStr
         !make_map(&mb, a.B, (uint64_t)a.G * kN, (uint64_t)a.T) ||
         !make_map(&mc, a.C, (uint64_t)a.G * kN, (uint64_t)a.T))
         return cudaErrorInvalidValue;
-    int32_t *order = static_cast<int32_t *>(workspace);
-    prep_order_kernel<<<1, kPrepThreads, 0, stream>>>(a.cu_seqlens, a.S, a.T, order);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *order = reinterpret_cast<int32_t *>(ws);
+    const WsLayout L = ws_layout(a.T, a.S, a.H);
+    const int hp = a.H / 2;
+    // Segments pay off only when the longest item is shorter than an SM's mean
+    // share of the work (the prep kernel decides from the actual lengths).  The
+    // host rules them out beforehand -- sparing the cooperative launch -- when
+    // the max_seqlen hint shows that the longest item is at least that share
+    // even for the largest block count T and S allow, or no longer than the
+    // shortest segment the prep kernel would choose.  A workspace without room
+    // for the states (the fixed-scratch entry point) runs unsegmented.
+    bool seg = L.cap > 0 && workspace_bytes >= L.total && (int64_t)a.S * hp > sms;
+    if (seg && a.max_seqlen > 0) {
+        const int64_t nb0 = ((int64_t)a.max_seqlen + kQ - 1) / kQ;
+        const int64_t tb = (a.T + kQ - 1) / kQ;
+        const int64_t min_seg = std::max<int64_t>(kSegMinBlocks, (tb * hp + (int64_t)kSegPerSm * sms - 1) / ((int64_t)kSegPerSm * sms));
+        if (nb0 * sms >= (tb + a.S) * hp || nb0 <= min_seg) seg = false;
+    }
+    int32_t *meta = seg ? reinterpret_cast<int32_t *>(ws + L.meta) : nullptr;
+    int32_t *bstart = seg ? reinterpret_cast<int32_t *>(ws + L.bstart) : nullptr;
+    int32_t *flags = seg ? reinterpret_cast<int32_t *>(ws + L.flags) : nullptr;
+    float *states = seg ? reinterpret_cast<float *>(ws + L.states) : nullptr;
+    prep_order_kernel<<<1, kPrepThreads, kPrepSmem, stream>>>(a.cu_seqlens, a.S, a.T, order, meta, bstart, flags,
+                                                               hp, sms, L.cap, seg ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     Params p;
@@ -1186,14 +1535,34 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, cudaStr
     p.cu_seqlens = a.cu_seqlens;
     p.slot_idx = a.slot_idx;
     p.order = order;
+    p.meta = meta;
+    p.bstart = bstart;
+    p.seg_flags = flags;
+    p.seg_state = states;
+    p.seg_enabled = seg ? 1 : 0;
     p.has_init = a.has_init;
     p.state_cache = a.state_cache;
     p.out_y = a.out_y;
     p.x = a.x;
     p.device_status = a.device_status;
     const int grid = p.num_items < sms ? p.num_items : sms;
-    chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
-    return cudaGetLastError();
+    if (!seg) {
+        chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
+        return cudaGetLastError();
+    }
+    // A segment waits for the CTA that runs the previous one, so every CTA
+    // must be resident at once: a cooperative launch (one CTA per SM).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunked_scan_kernel<StT>, mx, mb, mc, p);
 }
 
 }  // namespace
@@ -1211,14 +1580,15 @@ bool chunked_supported(const ssd_scan_params &p) {
 }
 
 size_t chunked_workspace_bytes(const ssd_scan_params &p) {
-    return ((size_t)p.num_seqs * sizeof(int32_t) + 255) & ~(size_t)255;
+    return ws_layout(p.total_tokens, p.num_seqs, p.nheads).total;
 }
 
-cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace, cudaStream_t stream) {
+cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
     switch (state_dtype) {
-        case SSD_F32: return launch_typed<float>(a, 0, workspace, stream);
-        case SSD_BF16: return launch_typed<__nv_bfloat16>(a, 1, workspace, stream);
-        case SSD_F16: return launch_typed<__half>(a, 2, workspace, stream);
+        case SSD_F32: return launch_typed<float>(a, 0, workspace, workspace_bytes, stream);
+        case SSD_BF16: return launch_typed<__nv_bfloat16>(a, 1, workspace, workspace_bytes, stream);
+        case SSD_F16: return launch_typed<__half>(a, 2, workspace, workspace_bytes, stream);
     }
     return cudaErrorInvalidValue;
 }

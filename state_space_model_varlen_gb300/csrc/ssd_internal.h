@@ -12,6 +12,7 @@ namespace ssd {
 struct ScanArgs {
     int64_t T;
     int32_t S, H, P, N, G;
+    int32_t max_seqlen;          // host hint (0 = unknown)
     int32_t heads_per_group;
     int32_t num_slots;
     int32_t dt_softplus, write_final;
@@ -28,11 +29,14 @@ struct ScanArgs {
 cudaError_t launch_recurrent(const ScanArgs &a, int io_dtype, int state_dtype,
                              cudaStream_t stream);
 
-// Chunked tcgen05 scan (bf16 I/O, P = 64, N = 128).  Two launches.
+// Chunked tcgen05 scan (bf16 I/O, P = 64, N = 128).  Two launches.  Long
+// sequences are cut into segments run by different CTAs when the workspace
+// holds chunked_workspace_bytes; a smaller one (at least 4 S bytes, the
+// sequence order) runs every sequence on one CTA.
 bool chunked_supported(const ssd_scan_params &p);
 size_t chunked_workspace_bytes(const ssd_scan_params &p);
 cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace,
-                           cudaStream_t stream);
+                           size_t workspace_bytes, cudaStream_t stream);
 
 namespace detail {
 // Host-side argument checks, launch arguments and kernel-path choice shared by

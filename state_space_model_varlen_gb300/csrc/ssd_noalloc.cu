@@ -65,7 +65,7 @@ extern "C" ssd_status ssd_scan_varlen_noalloc(const ssd_scan_params *params,
     if (ssd::detail::use_chunked(params)) {
         void *scratch = nullptr;
         err = scratch_for_current_device(&scratch);
-        if (err == cudaSuccess) err = ssd::launch_chunked(a, params->state_dtype, scratch, stream);
+        if (err == cudaSuccess) err = ssd::launch_chunked(a, params->state_dtype, scratch, sizeof(g_noalloc_scratch), stream);
     } else {
         err = ssd::launch_recurrent(a, params->io_dtype, params->state_dtype, stream);
     }

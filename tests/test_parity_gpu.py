@@ -242,3 +242,30 @@ def test_more_sequences_than_the_longest_first_sort_holds():
                        cache_std=0.1, seed=52)
     out, _ = _run_and_check(p)
     assert out["path"] == "chunked_tc"
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_segments_hand_over_the_state_between_ctas(state_dtype):
+    """Eight 2,900-5,200-token sequences x 40 head pairs (more items than SMs): the
+    prep kernel cuts each item into up to four 11-block segments run by different
+    CTAs, the state passing through the workspace in fp32.  Initial states from the
+    cache for half of the sequences, final states written back."""
+    rng = np.random.default_rng(53)
+    lens = rng.integers(2900, 5200, size=8)
+    p = W.make_problem(lens, nheads=80, headdim=64, dstate=128, ngroups=1, num_slots=12,
+                       has_init=[1, 0, 1, 0, 0, 1, 1, 0], cache_std=0.1, state_dtype=state_dtype,
+                       seed=53)
+    out = _sampled(p, [0, 2, 7], (24, 40))
+    assert out["path"] == "chunked_tc"
+
+
+def test_seven_segments_per_item():
+    """Four ~8,100-token sequences x 40 head pairs: 10-block segments, seven per
+    item (a chain of six hand-overs through the workspace), every sequence from
+    an initial state."""
+    rng = np.random.default_rng(54)
+    lens = rng.integers(8100, 8193, size=4)
+    p = W.make_problem(lens, nheads=80, headdim=64, dstate=128, ngroups=2, num_slots=6,
+                       has_init=True, cache_std=0.3, seed=54)
+    out = _sampled(p, [1, 3], (56, 72))
+    assert out["path"] == "chunked_tc"
