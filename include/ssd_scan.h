@@ -134,8 +134,11 @@ size_t ssd_scan_varlen_workspace_size(const ssd_scan_params *params);
  * SSD_ERR_CUDA.  Never synchronises. */
 ssd_status ssd_scan_varlen(const ssd_scan_params *params, struct CUstream_st *stream);
 
-/* Number of kernels a call with these parameters launches (0 for an empty
- * batch, at most 2), or -1 if the parameters are invalid. */
+/* Number of kernels a call with these parameters launches: 0 for an empty
+ * batch, else 1 or 2 (the tensor-core path sorts a batch of at most 32
+ * sequences that it does not cut into segments inside its one kernel; the
+ * choice depends on params->workspace_bytes and the current device's SM
+ * count).  -1 if the parameters are invalid or the device query fails. */
 int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params);
 
 /* Name of the kernel path a call would take: "chunked_tc" (tcgen05 chunked

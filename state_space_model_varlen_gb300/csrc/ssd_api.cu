@@ -92,7 +92,7 @@ size_t ssd_scan_varlen_workspace_size(const ssd_scan_params *params) {
 int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params) {
     if (validate(params) != SSD_OK) return -1;
     if (params->num_seqs == 0) return 0;
-    return use_chunked(params) ? 2 : 1;
+    return use_chunked(params) ? ssd::chunked_num_launches(*params, params->workspace_bytes) : 1;
 }
 
 const char *ssd_scan_varlen_path(const ssd_scan_params *params) {

@@ -82,6 +82,7 @@ constexpr int kMaxLevels = 32;                   // segments per item at most
 constexpr int kMetaInts = 64;                    // [0] items, [1] seg, [2] levels, [4 + j] level offsets
 constexpr int kSegMinBlocks = 6;                 // blocks per segment at least
 constexpr int kSegPerSm = 8;                     // segments per SM aimed at
+constexpr int kSegMaxItemsPerSm = 4;             // batches with more items per SM are not cut
 constexpr int kSegSlots = 1024;                  // handed-over states the workspace holds at most
 constexpr size_t kSegStateBytes = 2 * 64 * 128 * sizeof(float);   // one head pair's fp32 state
 
@@ -105,6 +106,7 @@ struct Params {
     int32_t *seg_flags;                           // per boundary, head pair and state warp: published
     float *seg_state;                             // per boundary and head pair: fp32 h [2][64][128]
     int32_t seg_enabled;
+    int32_t sort_in_cta;                          // S <= 32 and no prep launch: the item warp sorts
     const uint8_t *has_init;
     void *state_cache, *out_y;
     const void *x;
@@ -142,6 +144,7 @@ struct __align__(16) Item {
                                   // 3: final state to the workspace
 };
 constexpr int kItemRing = 8;      // items looked up ahead by the item warp
+constexpr int kSortInCta = 32;    // batches of up to this many sequences are sorted in the kernel
 constexpr uint32_t kItemTakers = 15;   // walkers per item: 2 single threads + 13 warps
 
 struct __align__(1024) Smem {
@@ -157,6 +160,7 @@ struct __align__(1024) Smem {
     uint64_t drain_y, drain_h;
     uint64_t item_full[kItemRing], item_empty[kItemRing];
     Item items[kItemRing];
+    int32_t order_small[kSortInCta];      // longest-first order when the item warp sorts
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -188,7 +192,7 @@ struct Chunk {
 // segment, ... -- so a segment's predecessor is always dealt earlier; the
 // sequences with a j-th segment are a prefix of the longest-first order.
 // Out of line: called once per item.
-__device__ __noinline__ Item find_item(const Params &p, int32_t round, bool report) {
+__device__ __noinline__ Item find_item(const Params &p, const int32_t *order, int32_t round, bool report) {
     Item it;
     it.flags = 0;
     const int32_t hp_per_seq = p.H / 2;
@@ -210,7 +214,7 @@ __device__ __noinline__ Item find_item(const Params &p, int32_t round, bool repo
         const int32_t r = idx - off;
         const int32_t rank = r / hp_per_seq;
         const int32_t hp = r - rank * hp_per_seq;
-        const int32_t seq = p.order[rank];
+        const int32_t seq = order[rank];
         const int32_t h0 = hp * 2;
         const int64_t a = p.cu_seqlens[seq], e = p.cu_seqlens[seq + 1];
         if (a < 0 || e < a || e > p.T) {
@@ -350,6 +354,29 @@ __device__ __noinline__ Item take_item(Smem &sm, uint32_t ik, bool whole_warp, i
     return it;
 }
 
+// Longest-first order of a batch of at most 32 sequences by a bitonic sort
+// over the lanes of one warp (keys as in the prep kernel).  Out of line and
+// compact: runs once per CTA.
+__device__ __noinline__ void sort_small(const Params &p, int32_t *order) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long key = ~0ull;
+    if (lane < p.S) {
+        const int64_t a = p.cu_seqlens[lane], e = p.cu_seqlens[lane + 1];
+        const int32_t v = (a < 0 || e < a || e > p.T) ? 0 : (int32_t)((e - a + kQ - 1) / kQ);
+        key = ((unsigned long long)(uint32_t)(0x7FFFFFFF - v) << 32) | (uint32_t)lane;
+    }
+#pragma unroll 1
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll 1
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, j);
+            key = (((lane & j) == 0) == ((lane & k) == 0)) ? (o < key ? o : key) : (o > key ? o : key);
+        }
+    }
+    order[lane] = (int32_t)(uint32_t)key;
+    __syncwarp();
+}
+
 // Walks this CTA's items block by block; identical in every role.  The items
 // come from a ring in shared memory that the item warp fills ahead of use,
 // so no role waits on the lookups' global loads at an item boundary.
@@ -448,7 +475,7 @@ template <> __device__ __forceinline__ void store_state<__half>(__half *p, float
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 1024;
 constexpr int kSortMax = 8192;
-constexpr int kPrepSmem = 2 * kSortMax * (int)sizeof(int32_t);   // dynamic shared memory of the prep kernel
+constexpr int kPrepSmem = kSortMax * (int)sizeof(unsigned long long);   // dynamic shared memory of the prep kernel
 
 // Longest-first order of the sequences (by block count), and, when enabled,
 // their cut into segments: seg blocks per segment, chosen so that about
@@ -464,9 +491,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
                                                                     int32_t *order, int32_t *meta,
                                                                     int32_t *bstart, int32_t *flags, int hp,
                                                                     int num_sms, int cap, int seg_enabled) {
-    extern __shared__ int32_t prep_smem[];
-    int32_t *nb = prep_smem;                     // block count by sequence
-    int32_t *nbr = prep_smem + kSortMax;         // block count by rank
+    // sort keys: (2^31 - 1 - block count) << 32 | sequence, ascending = longest
+    // first, ties by sequence index
+    extern __shared__ unsigned long long keys[];
+    auto nbr = [&](int r) { return 0x7FFFFFFF - (int32_t)(keys[r] >> 32); };   // block count by rank
     __shared__ int32_t part[kPrepThreads / 32];
     __shared__ uint32_t total;                   // blocks of all sequences (< 2^25 here)
     __shared__ int32_t seg_s;
@@ -474,23 +502,38 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
         for (int s = threadIdx.x; s < S; s += blockDim.x) order[s] = s;
         return;
     }
-    for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        const int64_t a = cu[s], e = cu[s + 1];
-        nb[s] = (a < 0 || e < a || e > T) ? 0 : (int32_t)((e - a + kQ - 1) / kQ);
+    int p2 = 1;                                  // bitonic sort over a power of two
+    while (p2 < S) p2 <<= 1;
+    for (int s = threadIdx.x; s < p2; s += blockDim.x) {
+        unsigned long long key = ~0ull;          // padding sorts last
+        if (s < S) {
+            const int64_t a = cu[s], e = cu[s + 1];
+            const int32_t v = (a < 0 || e < a || e > T) ? 0 : (int32_t)((e - a + kQ - 1) / kQ);
+            key = ((unsigned long long)(uint32_t)(0x7FFFFFFF - v) << 32) | (uint32_t)s;
+        }
+        keys[s] = key;
     }
     if (threadIdx.x == 0) total = 0;
     __syncthreads();
-    uint32_t mine = 0;
-    for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        const int32_t v = nb[s];
-        int rank = 0;
-        for (int q = 0; q < S; ++q) {
-            const int32_t u = nb[q];
-            rank += (u > v) || (u == v && q < s);
+    for (int k = 2; k <= p2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long x = keys[i], y = keys[l];
+                    if ((x > y) == ((i & k) == 0)) {
+                        keys[i] = y;
+                        keys[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
         }
-        order[rank] = s;
-        nbr[rank] = v;
-        mine += v;
+    }
+    uint32_t mine = 0;
+    for (int r = threadIdx.x; r < S; r += blockDim.x) {
+        order[r] = (int32_t)(uint32_t)keys[r];
+        mine += nbr(r);
     }
     if (!seg_enabled) return;
     mine = __reduce_add_sync(0xffffffffu, mine);
@@ -502,11 +545,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
         // Only when the longest item is shorter than an SM's mean share: a
         // longer one is the critical path already, and its segments would run
         // one after another anyway.
-        if (cap > 0 && (long long)nbr[0] * num_sms < work) {
+        if (cap > 0 && (long long)nbr(0) * num_sms < work) {
             // boundaries x hp <= total x hp / seg <= cap
             long long v = max((long long)kSegMinBlocks, (work + (long long)kSegPerSm * num_sms - 1) / ((long long)kSegPerSm * num_sms));
             v = max(v, (work + cap - 1) / cap);
-            v = max(v, (long long)(nbr[0] + kMaxLevels - 1) / kMaxLevels);
+            v = max(v, (long long)(nbr(0) + kMaxLevels - 1) / kMaxLevels);
             seg = (int)min(v, 0x40000000LL);
         }
         seg_s = seg;
@@ -519,7 +562,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
     int32_t local = 0;
     for (int k = 0; k < kPer; ++k) {
         const int r = r0 + k;
-        if (r < S) local += nbr[r] == 0 ? 0 : (nbr[r] + seg - 1) / seg - 1;
+        if (r < S) local += nbr(r) == 0 ? 0 : (nbr(r) + seg - 1) / seg - 1;
     }
     // block-wide exclusive scan of `local`
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -544,13 +587,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
         const int r = r0 + k;
         if (r < S) {
             bstart[r] = run;
-            run += nbr[r] == 0 ? 0 : (nbr[r] + seg - 1) / seg - 1;
+            run += nbr(r) == 0 ? 0 : (nbr(r) + seg - 1) / seg - 1;
         }
     }
     const int32_t nbound = part[31];
     for (int i = threadIdx.x; i < nbound * hp * 4; i += blockDim.x) flags[i] = 0;
     if (threadIdx.x == 0) {
-        const int nlev = nbr[0] == 0 ? 1 : (nbr[0] + seg - 1) / seg;
+        const int nlev = nbr(0) == 0 ? 1 : (nbr(0) + seg - 1) / seg;
         // sequences with a j-th segment are the first cnt_j ranks (block counts are sorted)
         int32_t offs = 0;
         for (int j = 0; j < nlev; ++j) {
@@ -558,7 +601,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
             int lo = 0, hi = S;                  // first rank whose item has no j-th segment
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
-                const int ns = nbr[mid] == 0 ? 1 : (nbr[mid] + seg - 1) / seg;
+                const int ns = nbr(mid) == 0 ? 1 : (nbr(mid) + seg - 1) / seg;
                 if (ns > j) lo = mid + 1; else hi = mid;
             }
             offs += lo * hp;
@@ -883,6 +926,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         // Looks this CTA's items up in deal order (one thread) and hands them to
         // the walkers of every role through the ring, up to kItemRing ahead;
         // the last entry is the end marker.
+        const int32_t *order = p.order;
+        if (p.sort_in_cta) {
+            sort_small(p, sm.order_small);
+            order = sm.order_small;
+        }
         if (lane == 0) {
             int32_t round = 0;
             for (uint32_t k = 0;; ++k) {
@@ -890,7 +938,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 if (k >= (uint32_t)kItemRing &&
                     !wait_bar(sm, &sm.item_empty[s], ((k / kItemRing) - 1) & 1, status))
                     break;
-                const Item it = find_item(p, round, true);
+                const Item it = find_item(p, order, round, true);
                 round = it.round;
                 sm.items[s] = it;
                 mbar_arrive(&sm.item_full[s]);
@@ -957,7 +1005,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             // ---- hi part bf16(w x) into the buffer once block k-1's lo MMA has read it ----
             ok = ok && (kc == 0 || warp_wait(sm, &sm.xbuf_free, 1, status));
             if (ok) {
-#pragma unroll 1
+#pragma unroll 4
             for (int i = 0; i < 16; ++i) {
                 const int hh = i >> 3, cc = i & 7;
                 const float2 ww = hh ? make_float2(w1, w1) : make_float2(w0, w0);
@@ -1458,6 +1506,45 @@ WsLayout ws_layout(int64_t T, int32_t S, int32_t H) {
     return L;
 }
 
+// Segments pay off only when there are few items per SM (with more, the
+// longest-first deal already balances the SMs) and the longest item is
+// shorter than an SM's mean share of the work (the prep kernel decides that
+// from the actual lengths).  The host rules them out beforehand -- sparing the
+// cooperative launch -- when the max_seqlen hint shows that the longest item
+// is at least that share even for the largest block count T and S allow, or no
+// longer than the shortest segment the prep kernel would choose.  A workspace
+// without room for the states (the fixed-scratch entry point) runs unsegmented.
+bool may_segment(int64_t T, int32_t S, int32_t H, int32_t max_seqlen, size_t workspace_bytes, int sms) {
+    const WsLayout L = ws_layout(T, S, H);
+    const int64_t hp = H / 2;
+    const int64_t items = (int64_t)S * hp;
+    if (!(L.cap > 0 && workspace_bytes >= L.total && items > sms && items < (int64_t)kSegMaxItemsPerSm * sms))
+        return false;
+    if (max_seqlen > 0) {
+        const int64_t nb0 = ((int64_t)max_seqlen + kQ - 1) / kQ;
+        const int64_t tb = (T + kQ - 1) / kQ;
+        const int64_t per = (int64_t)kSegPerSm * sms;
+        const int64_t min_seg = std::max<int64_t>(kSegMinBlocks, (tb * hp + per - 1) / per);
+        if (nb0 * sms >= (tb + S) * hp || nb0 <= min_seg) return false;
+    }
+    return true;
+}
+
+cudaError_t current_device_sms(int *sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (di.sms == 0) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *sms = di.sms;
+    return cudaSuccess;
+}
+
 template <typename StT>
 cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
@@ -1495,28 +1582,19 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
     int32_t *order = reinterpret_cast<int32_t *>(ws);
     const WsLayout L = ws_layout(a.T, a.S, a.H);
     const int hp = a.H / 2;
-    // Segments pay off only when the longest item is shorter than an SM's mean
-    // share of the work (the prep kernel decides from the actual lengths).  The
-    // host rules them out beforehand -- sparing the cooperative launch -- when
-    // the max_seqlen hint shows that the longest item is at least that share
-    // even for the largest block count T and S allow, or no longer than the
-    // shortest segment the prep kernel would choose.  A workspace without room
-    // for the states (the fixed-scratch entry point) runs unsegmented.
-    bool seg = L.cap > 0 && workspace_bytes >= L.total && (int64_t)a.S * hp > sms;
-    if (seg && a.max_seqlen > 0) {
-        const int64_t nb0 = ((int64_t)a.max_seqlen + kQ - 1) / kQ;
-        const int64_t tb = (a.T + kQ - 1) / kQ;
-        const int64_t min_seg = std::max<int64_t>(kSegMinBlocks, (tb * hp + (int64_t)kSegPerSm * sms - 1) / ((int64_t)kSegPerSm * sms));
-        if (nb0 * sms >= (tb + a.S) * hp || nb0 <= min_seg) seg = false;
-    }
+    const bool seg = may_segment(a.T, a.S, a.H, a.max_seqlen, workspace_bytes, sms);
     int32_t *meta = seg ? reinterpret_cast<int32_t *>(ws + L.meta) : nullptr;
     int32_t *bstart = seg ? reinterpret_cast<int32_t *>(ws + L.bstart) : nullptr;
     int32_t *flags = seg ? reinterpret_cast<int32_t *>(ws + L.flags) : nullptr;
     float *states = seg ? reinterpret_cast<float *>(ws + L.states) : nullptr;
-    prep_order_kernel<<<1, kPrepThreads, kPrepSmem, stream>>>(a.cu_seqlens, a.S, a.T, order, meta, bstart, flags,
-                                                               hp, sms, L.cap, seg ? 1 : 0);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // Small unsegmented batches are sorted by the scan kernel itself: one launch.
+    const bool sort_in_cta = !seg && a.S <= kSortInCta;
+    if (!sort_in_cta) {
+        prep_order_kernel<<<1, kPrepThreads, kPrepSmem, stream>>>(a.cu_seqlens, a.S, a.T, order, meta, bstart,
+                                                                   flags, hp, sms, L.cap, seg ? 1 : 0);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     Params p;
     p.T = a.T;
     p.S = a.S;
@@ -1540,6 +1618,7 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
     p.seg_flags = flags;
     p.seg_state = states;
     p.seg_enabled = seg ? 1 : 0;
+    p.sort_in_cta = sort_in_cta ? 1 : 0;
     p.has_init = a.has_init;
     p.state_cache = a.state_cache;
     p.out_y = a.out_y;
@@ -1581,6 +1660,13 @@ bool chunked_supported(const ssd_scan_params &p) {
 
 size_t chunked_workspace_bytes(const ssd_scan_params &p) {
     return ws_layout(p.total_tokens, p.num_seqs, p.nheads).total;
+}
+
+int32_t chunked_num_launches(const ssd_scan_params &p, size_t workspace_bytes) {
+    int sms = 0;
+    if (current_device_sms(&sms) != cudaSuccess) return -1;
+    const bool seg = may_segment(p.total_tokens, p.num_seqs, p.nheads, p.max_seqlen, workspace_bytes, sms);
+    return (!seg && p.num_seqs <= kSortInCta) ? 1 : 2;
 }
 
 cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace, size_t workspace_bytes,

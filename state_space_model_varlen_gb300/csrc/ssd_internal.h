@@ -29,7 +29,7 @@ struct ScanArgs {
 cudaError_t launch_recurrent(const ScanArgs &a, int io_dtype, int state_dtype,
                              cudaStream_t stream);
 
-// Chunked tcgen05 scan (bf16 I/O, P = 64, N = 128).  Two launches.  Long
+// Chunked tcgen05 scan (bf16 I/O, P = 64, N = 128).  One or two launches.  Long
 // sequences are cut into segments run by different CTAs when the workspace
 // holds chunked_workspace_bytes; a smaller one (at least 4 S bytes, the
 // sequence order) runs every sequence on one CTA.
@@ -37,6 +37,10 @@ bool chunked_supported(const ssd_scan_params &p);
 size_t chunked_workspace_bytes(const ssd_scan_params &p);
 cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace,
                            size_t workspace_bytes, cudaStream_t stream);
+// Launches of a chunked call with this workspace size on the current device
+// (1 when the kernel sorts a small unsegmented batch itself, else 2; -1 on a
+// CUDA error).
+int32_t chunked_num_launches(const ssd_scan_params &p, size_t workspace_bytes);
 
 namespace detail {
 // Host-side argument checks, launch arguments and kernel-path choice shared by

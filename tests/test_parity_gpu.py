@@ -179,12 +179,17 @@ def test_workload_mtp_sampled():
 
 
 def test_tensor_core_path_is_taken_for_bf16_prefill():
-    """bf16 I/O with headdim 64 / d_state 128 runs the two-launch tcgen05 path."""
+    """bf16 I/O with headdim 64 / d_state 128 runs the tcgen05 path: one launch for a
+    batch of at most 32 sequences (sorted inside the scan kernel), two beyond."""
     p = W.make_problem([200, 64], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
                        seed=45)
     out, _ = _run_and_check(p)
     assert out["path"] == "chunked_tc"
-    assert out["launches"] == 2
+    assert out["launches"] == 1
+    r = W.make_problem(np.arange(33) * 3 + 1, nheads=4, headdim=64, dstate=128, ngroups=2,
+                       num_slots=33, seed=56)
+    outr, _ = _run_and_check(r)
+    assert outr["path"] == "chunked_tc" and outr["launches"] == 2
     q = W.make_problem([3, 3], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
                        has_init=True, seed=46)
     outq = Hn.run_gpu(q, max_seqlen=3)
@@ -268,4 +273,17 @@ def test_seven_segments_per_item():
     p = W.make_problem(lens, nheads=80, headdim=64, dstate=128, ngroups=2, num_slots=6,
                        has_init=True, cache_std=0.3, seed=54)
     out = _sampled(p, [1, 3], (56, 72))
+    assert out["path"] == "chunked_tc"
+
+
+def test_longest_first_sort_of_thousands_of_sequences():
+    """3,000 sequences of 1-300 tokens (many equal block counts): the prep kernel's
+    bitonic sort over 4,096 keys (padded) orders them longest first; every output
+    and final state is compared."""
+    rng = np.random.default_rng(55)
+    lens = rng.integers(1, 41, size=3000)
+    lens[::97] = rng.integers(200, 301, size=lens[::97].shape[0])
+    p = W.make_problem(lens, nheads=2, headdim=64, dstate=128, ngroups=1, num_slots=3000,
+                       has_init=(rng.random(3000) < 0.3).astype(np.uint8), cache_std=0.1, seed=55)
+    out, _ = _run_and_check(p)
     assert out["path"] == "chunked_tc"
