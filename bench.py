@@ -79,11 +79,18 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# The sources the tensor-core scan kernel is compiled from (its translation unit
+# and the headers it includes): a DRAM-traffic capture stays valid while they do.
+_SCAN_KERNEL_SOURCES = ("state_space_model_varlen_gb300/csrc/sm100.cuh",
+                        "state_space_model_varlen_gb300/csrc/ssd_chunked.cu",
+                        "state_space_model_varlen_gb300/csrc/ssd_internal.h",
+                        "include/ssd_scan.h")
+
+
 def _kernel_source_digest() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "state_space_model_varlen_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for name in _SCAN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 

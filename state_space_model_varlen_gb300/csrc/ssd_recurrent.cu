@@ -98,8 +98,11 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 // kDepth: tokens of input prefetched ahead of the recurrence (a register ring;
 // deeper for narrow states, where registers are cheap and the chain is short).
+// Wide states (plain loop) are latency-bound on their few tokens per CTA:
+// twelve resident CTAs per SM (40 registers, a few spills to L1) keep more
+// loads and stores in flight than seven CTAs of 72 registers (MTP: -12 %).
 template <typename IoT, typename StT, int NPL, int kDepth>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, kDepth > 1 ? 1 : 12)
 recurrent_scan_kernel(ScanArgs a, bool vec) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -112,19 +115,20 @@ recurrent_scan_kernel(ScanArgs a, bool vec) {
     if (p0 >= a.P) return;                                   // warp-uniform
     const int g = h / a.heads_per_group;
 
-    // ---- sequence metadata, checked on the device --------------------------
+    // ---- sequence metadata, checked on the device (loads issued together) ----
     const int64_t t0 = a.cu_seqlens[s];
     const int64_t t1 = a.cu_seqlens[s + 1];
+    const bool init = a.has_init != nullptr && a.has_init[s] != 0;
+    const int slot_raw = a.slot_idx != nullptr ? a.slot_idx[s] : 0;
     if (t0 < 0 || t1 < t0 || t1 > a.T) {
         if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
             atomicOr(a.device_status, SSD_DEV_BAD_SEQLENS);
         return;
     }
-    const bool init = a.has_init != nullptr && a.has_init[s] != 0;
     const bool need_slot = init || a.write_final;
     int slot = 0;
     if (need_slot) {
-        slot = a.slot_idx[s];
+        slot = slot_raw;
         if (slot < 0 || slot >= a.num_slots) {
             if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
                 atomicOr(a.device_status, SSD_DEV_BAD_SLOT);
