@@ -76,7 +76,8 @@ __device__ __forceinline__ void store_n(T *dst, const float (&v)[NPL], int valid
             reinterpret_cast<uint4 *>(dst)[1] = reinterpret_cast<const uint4 *>(tmp)[1];
             return;
         } else if constexpr (bytes == 16) {
-            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(tmp);
+            // states are written once and not read again here: streaming store
+            __stcs(reinterpret_cast<uint4 *>(dst), *reinterpret_cast<const uint4 *>(tmp));
             return;
         } else if constexpr (bytes == 8) {
             *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(tmp);
@@ -98,12 +99,8 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 // kDepth: tokens of input prefetched ahead of the recurrence (a register ring;
 // deeper for narrow states, where registers are cheap and the chain is short).
-// Wide states (plain loop) are latency-bound on their few tokens per CTA:
-// twelve resident CTAs per SM (40 registers, a few spills to L1) keep more
-// loads and stores in flight than seven CTAs of 72 registers (MTP: -12 %).
 template <typename IoT, typename StT, int NPL, int kDepth>
-__global__ void __launch_bounds__(kWarps * 32, kDepth > 1 ? 1 : 12)
-recurrent_scan_kernel(ScanArgs a, bool vec) {
+__device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int pblocks = (a.P + kRowsPerCta - 1) / kRowsPerCta;
@@ -291,6 +288,20 @@ recurrent_scan_kernel(ScanArgs a, bool vec) {
     }
 }
 
+template <typename IoT, typename StT, int NPL, int kDepth>
+__global__ void __launch_bounds__(kWarps * 32) recurrent_scan_kernel(ScanArgs a, bool vec) {
+    recurrent_scan<IoT, StT, NPL, kDepth>(a, vec);
+}
+
+// The plain loop with four state columns per lane (N <= 128) is latency-bound
+// on its few tokens per CTA: twelve resident CTAs per SM (40 registers, a few
+// spills to L1) keep more loads and stores in flight than seven CTAs of 72
+// registers (MTP: -12 %).
+template <typename IoT, typename StT>
+__global__ void __launch_bounds__(kWarps * 32, 12) recurrent_scan_kernel_n4(ScanArgs a, bool vec) {
+    recurrent_scan<IoT, StT, 4, 1>(a, vec);
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <typename IoT, typename StT, int NPL>
@@ -300,7 +311,10 @@ cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t st
     const bool vec = (a.N % NPL == 0) && (a.P % kRowsPerWarp == 0) && aligned16(a.x) &&
                      aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
                      aligned16(a.out_intermediate);
-    recurrent_scan_kernel<IoT, StT, NPL, kDepth><<<grid, block, 0, stream>>>(a, vec);
+    if constexpr (NPL == 4 && kDepth == 1)
+        recurrent_scan_kernel_n4<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
+    else
+        recurrent_scan_kernel<IoT, StT, NPL, kDepth><<<grid, block, 0, stream>>>(a, vec);
     return cudaGetLastError();
 }
 
