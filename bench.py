@@ -87,11 +87,36 @@ _SCAN_KERNEL_SOURCES = ("state_space_model_varlen_gb300/csrc/sm100.cuh",
                         "include/ssd_scan.h")
 
 
+def _strip_comments(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed (string
+    and character literals kept), so that editing a comment keeps the digest."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def _kernel_source_digest() -> str:
     h = hashlib.sha256()
     for name in _SCAN_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(ROOT, name), encoding="utf-8") as f:
+            h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

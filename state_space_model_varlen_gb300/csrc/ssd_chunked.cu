@@ -8,11 +8,15 @@
 // than gathered into a dense buffer (vLLM PR #62922 "Details").  This file is
 // a single-pass design of the same computation for one GB300 SM:
 //
-// Launch 1 (prep): sort the sequences by block count, longest first, into the
-//   workspace (the only scratch memory), so the persistent CTAs below take
-//   the long chains first.
-// Launch 2 (scan): one persistent CTA per SM.  A work item is one sequence and
-//   two heads of the same B/C group; its tokens are walked in 128-token blocks.
+// Launch 1 (prep, skipped for unsegmented batches of <= 32 sequences, which the
+//   scan kernel sorts itself): sort the sequences by block count, longest
+//   first, into the workspace, so the persistent CTAs below take the long
+//   chains first; when a batch has few items per SM, also plan the cut of
+//   each item into segments run by different CTAs.
+// Launch 2 (scan): one persistent CTA per SM.  A work item is one sequence (or
+//   one segment of it) and two heads of the same B/C group; its tokens are
+//   walked in 128-token blocks.  A segment's initial state is the fp32 state
+//   the previous segment's CTA hands over through the workspace.
 //   The recurrent state h [2 heads x 64 x 128] never leaves the SM: it lives in
 //   tensor memory as an fp32 MMA accumulator.  Per block, with
 //   cum_t = sum_{r<=t} dt'_r A (within the block) and Xw_s = exp(cum_end - cum_s) dt'_s x_s:
@@ -37,8 +41,11 @@
 // and the state scales two blocks ahead; warps 4-7 (lane = token) build the
 // scaled Xw and issue the state MMAs (B^T Xw); warps 8-11 (lane = token) build
 // S and scale the rows of Y; warps 12-15 own the state (lane = state column n:
-// bf16 copy for C h^T, cache I/O) and write y of the previous block; warp 3 has
-// no role.  Hand-offs are mbarriers (and one named barrier inside warps 4-7);
+// bf16 copy for C h^T, cache I/O) and write y of the previous block; warp 3
+// looks the CTA's items up ahead of use and hands them to the other roles
+// through a ring in shared memory.  Hand-offs are mbarriers (and one named
+// barrier inside warps 4-7; release/acquire flags in global memory between
+// segments);
 // every wait is bounded and sets an abort flag plus SSD_DEV_TIMEOUT in
 // device_status instead of hanging.
 //
