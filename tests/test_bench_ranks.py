@@ -40,3 +40,12 @@ def test_max_over_ranks_gloo_world2():
 def test_whole_job_rate_counts_all_ranks():
     assert bench.whole_job_rate(1000, 4, 2.0) == pytest.approx(2e6)
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]     # single process: identity
+
+
+def test_traffic_digest_ignores_comments_only():
+    """The DRAM-traffic line is keyed by the scan kernel's sources without
+    comments: editing a comment keeps it, changing code does not."""
+    src = 'int a = 1; // note\n/* block\n comment */ const char *s = "x//y";\n'
+    assert bench._strip_comments(src) == 'int a = 1; const char *s = "x//y";'
+    assert bench._strip_comments(src.replace("note", "other note")) == bench._strip_comments(src)
+    assert bench._strip_comments(src.replace("a = 1", "a = 2")) != bench._strip_comments(src)
