@@ -287,3 +287,31 @@ def test_longest_first_sort_of_thousands_of_sequences():
                        has_init=(rng.random(3000) < 0.3).astype(np.uint8), cache_std=0.1, seed=55)
     out, _ = _run_and_check(p)
     assert out["path"] == "chunked_tc"
+
+
+def test_segments_with_an_empty_sequence_and_a_bad_slot():
+    """A batch the prep kernel cuts into segments that also holds an empty
+    sequence and one whose slot is out of range: the bad sequence is skipped in
+    every segment (its y rows stay unwritten, the device status says so), the
+    empty one gets its slot zeroed, and the others match the oracle."""
+    rng = np.random.default_rng(57)
+    lens = rng.integers(2900, 5200, size=9)
+    lens[4] = 0
+    slots = list(range(9))
+    slots[6] = 40                                   # outside [0, num_slots)
+    p = W.make_problem(lens, nheads=80, headdim=64, dstate=128, ngroups=1, num_slots=12,
+                       slots=slots, has_init=[1, 0, 1, 0, 0, 1, 0, 0, 1], cache_std=0.1, seed=57)
+    out = Hn.run_gpu(p)
+    assert out["status"] & 1 and out["path"] == "chunked_tc"
+    cu = p.cu_seqlens
+    assert np.all(np.isnan(out["y"][cu[6]:cu[7]]))
+    np.testing.assert_array_equal(out["cache"][4], np.zeros_like(out["cache"][4]))
+    good = [0, 3, 8]
+    q = W.select_sequences(p, good)
+    ref = oracle.ssd_scan_reference(q, heads=(40, 56))
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in good])
+    Hn.check_y(out["y"][rows][:, 40:56], ref["y"][:, 40:56], p.io_dtype)
+    for j, s in enumerate(good):
+        Hn.check_state(out["cache"][p.slot_idx[s], 40:56], ref["final"][j, 40:56], p.state_dtype)
+    untouched = [i for i in range(p.num_slots) if i not in set(slots)]
+    np.testing.assert_array_equal(out["cache"][untouched], p.cache[untouched])
