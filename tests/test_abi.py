@@ -102,3 +102,27 @@ def test_status_strings():
     for code in range(5):
         assert binding.status_string(code) and binding.status_string(code) != "unknown status"
     assert binding.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("S,H,expect", [
+    (2, 4, 256),                  # no hand-over possible: the sequence order only
+    (40, 2, 394240),              # 6 hand-over states (6-block segments bound them)
+    (600, 80, 67130624),          # 1024 hand-over states at most
+    (8193, 80, 33024),            # beyond the sort: the sequence order only
+])
+def test_workspace_layout(S, H, expect):
+    """Workspace of the tensor-core path (T = 0 keeps the query on the host):
+    int32 order[S], then for segments a 64-int level table, int32 bstart[S],
+    four flags and one 64 KiB fp32 state per hand-over, each part 256-byte
+    aligned."""
+    p = _params(total_tokens=0, num_seqs=S, nheads=H, ngroups=1)
+    assert binding.kernel_path(p) == "chunked_tc"
+    r256 = lambda v: (v + 255) // 256 * 256
+    size = binding.workspace_size(p)
+    assert size == expect
+    cap = min(1024, S * (H // 2) // 6)
+    if S <= 8192 and cap > 0:
+        assert size == r256(4 * S) + 256 + r256(4 * S) + r256(16 * cap) + cap * 65536
+    else:
+        assert size == r256(4 * S)
+    assert size <= r256(4 * S) * 2 + 256 + 16384 + (64 << 20)
