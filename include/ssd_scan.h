@@ -39,7 +39,10 @@
  * Ownership: the caller owns every buffer.  The library allocates nothing,
  * frees nothing and never synchronises: a call validates its arguments on
  * the host, enqueues at most two kernels on `stream` and returns.  Nothing is
- * read back to the host, so a call may be captured in a CUDA graph.
+ * read back to the host, so a call may be captured in a CUDA graph.  A batch
+ * the tensor-core path cuts into segments is launched cooperatively (its CTAs
+ * hand states to one another); where the context has fewer SMs than the
+ * device, that launch falls back to running every sequence whole.
  *
  * Aliasing: state_cache is read (initial states) and written (final states)
  * in place; a sequence's final state goes into the slot its initial state

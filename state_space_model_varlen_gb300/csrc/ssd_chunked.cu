@@ -1648,7 +1648,14 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunked_scan_kernel<StT>, mx, mb, mc, p);
+    e = cudaLaunchKernelEx(&cfg, chunked_scan_kernel<StT>, mx, mb, mc, p);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    // Fewer SMs available to this context than the grid (a partitioned GPU):
+    // run every item whole instead; the prep kernel's order stays valid.
+    (void)cudaGetLastError();
+    p.seg_enabled = 0;
+    chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
