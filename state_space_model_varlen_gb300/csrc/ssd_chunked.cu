@@ -22,26 +22,29 @@
 //   cum_t = sum_{r<=t} dt'_r A (within the block) and Xw_s = exp(cum_end - cum_s) dt'_s x_s:
 //     G   = C B^T                          tcgen05, fp32 in TMEM
 //     S_h = G o exp(cum_t - cum_s) dt'_s   (s <= t) bf16, written back in TMEM
-//     Y   = C h^T                          tcgen05, state entering the block (bf16 copy)
+//     Y   = C h^T                          tcgen05, state entering the block as two
+//                                          bf16 parts hi + lo (h - hi), so the fp32
+//                                          state enters y at fp32-like accuracy
 //     Y  *= exp(cum_t)                     per row and head, in TMEM
 //     Y  += S_h X_h                        tcgen05, A operand from TMEM
 //     y   = Y + D x                        bf16
 //     h   = exp(cum_end) h + B^T Xw        tcgen05 accumulating into the state,
 //                                          Xw split into bf16 hi + lo
-//   The hi/lo split keeps the state contributions accurate to ~2^-16, so final
-//   states meet fp32-storage accuracy; the y path runs on bf16 operands with
-//   fp32 accumulation.  The state is accumulated in a scaled form with a
+//   The hi/lo splits keep the state contributions and the state's part of y
+//   accurate to ~2^-16, so final states meet fp32-storage accuracy and an fp32
+//   initial state reaches y without a bf16 rounding; the intra-block y path
+//   runs on bf16 operands with fp32 accumulation.  The state is accumulated in a scaled form with a
 //   running per-head scale, so a block needs no rescaling pass over it.  Y is
 //   double buffered in TMEM so block k+1's C h^T can start while block k's
 //   epilogue drains.
 //
 // Warp roles (16 warps): warp 0 TMA producer (C, B, X tiles of 128 tokens,
-// 5-slot ring); warp 1 issues the output-path MMAs (G, C h^T, S X); warp 2
+// 4-slot ring); warp 1 issues the output-path MMAs (G, C h^T, S X); warp 2
 // owns the TMEM allocation and computes dt softplus, the within-block cumsum
 // and the state scales two blocks ahead; warps 4-7 (lane = token) build the
 // scaled Xw and issue the state MMAs (B^T Xw); warps 8-11 (lane = token) build
 // S and scale the rows of Y; warps 12-15 own the state (lane = state column n:
-// bf16 copy for C h^T, cache I/O) and write y of the previous block; warp 3
+// bf16 hi/lo copies for C h^T, cache I/O) and write y of the previous block; warp 3
 // looks the CTA's items up ahead of use and hands them to the other roles
 // through a ring in shared memory.  Hand-offs are mbarriers (and one named
 // barrier inside warps 4-7; release/acquire flags in global memory between
@@ -72,7 +75,7 @@ using namespace sm100;
 constexpr int kQ = 128;            // tokens per block
 constexpr int kP = 64;             // head dim
 constexpr int kN = 128;            // state dim
-constexpr int kSlots = 5;          // TMA ring of 32 KB tiles (C, B, X per block)
+constexpr int kSlots = 4;          // TMA ring of 32 KB tiles (C, B, X per block)
 constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kHbufHead = 8192;    // one head of the half-n bf16 state copy: 64 rows x 128 B
@@ -157,12 +160,13 @@ constexpr uint32_t kItemTakers = 15;   // walkers per item: 2 single threads + 1
 struct __align__(1024) Smem {
     uint8_t slot[kSlots][kTileBytes];     // TMA ring: C / B [n half][s][n], X [head][s][p]
     uint8_t xw[2][kHalfBytes];            // Xw (hi, then lo), [head][s][p], 128-B swizzle
-    uint8_t hbuf[2 * kHbufHead];          // bf16 h, one half of n at a time: [head][n % 64][p]
+    uint8_t hbuf[2 * kHbufHead];          // bf16 h (hi part), one half of n at a time: [head][n % 64][p]
+    uint8_t hlo[2][2 * kHbufHead];        // bf16 h - hi (lo part), all n: [n / 64][head][n % 64][p]
     Arrays arr[kArrBufs];
     uint64_t full[kSlots], empty[kSlots];
     uint64_t arr_ready[kArrBufs], arr_free[kArrBufs];
     uint64_t g_ready, s_ready, xbuf_free;
-    uint64_t hs_a, hs_b, hbuf_a_done, state_ok, state_done;
+    uint64_t hs_a, hs_b, hbuf_a_done, hlo_ready, hlo_free, state_ok, state_done;
     uint64_t yinter_ready, y_scaled, y_ready[2], y_free[2], x_epi_done[2];
     uint64_t drain_y, drain_h;
     uint64_t item_full[kItemRing], item_empty[kItemRing];
@@ -177,7 +181,8 @@ static_assert(sizeof(Arrays) % 16 == 0, "Arrays must keep float4 rows aligned");
 static_assert(offsetof(Arrays, dtp) % 16 == 0 && offsetof(Arrays, vfac) % 16 == 0 &&
               offsetof(Arrays, vdiag) % 16 == 0, "Arrays rows must be 16-byte aligned");
 static_assert(offsetof(Smem, arr) % 16 == 0, "Arrays must start 16-byte aligned");
-static_assert(offsetof(Smem, xw) % 1024 == 0 && offsetof(Smem, hbuf) % 1024 == 0,
+static_assert(offsetof(Smem, xw) % 1024 == 0 && offsetof(Smem, hbuf) % 1024 == 0 &&
+              offsetof(Smem, hlo) % 1024 == 0,
               "swizzled operand tiles must be 1024-byte aligned");
 
 // ---------------------------------------------------------------------------
@@ -789,6 +794,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         mbar_init(&sm.hs_a, 2);
         mbar_init(&sm.hs_b, 2);
         mbar_init(&sm.hbuf_a_done, 1);
+        mbar_init(&sm.hlo_ready, 4);
+        mbar_init(&sm.hlo_free, 1);
         mbar_init(&sm.state_ok, 4);
         mbar_init(&sm.state_done, 1);
         mbar_init(&sm.yinter_ready, 1);
@@ -874,7 +881,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 tc_fence_after();
                 {
                     const uint64_t dc = smem_desc_sw128(bC, 16, 1024), db = smem_desc_sw128(bB, 16, 1024);
-#pragma unroll 1
+#pragma unroll
                     for (uint32_t ks = 0; ks < 8; ++ks) {
                         const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
                         mma_ss(tmem + kColG, dc + off, db + off, kIdG, ks > 0);
@@ -889,7 +896,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 tc_fence_after();
                 {
                     const uint64_t dc = smem_desc_sw128(bC, 16, 1024), dh = smem_desc_sw128(bH, kHbufHead, 1024);
-#pragma unroll 1
+#pragma unroll
                     for (uint32_t ks = 0; ks < 4; ++ks)
                         mma_ss(tmem + ycol, dc + ks * 2, dh + ks * 128, kIdY, ks > 0);
                 }
@@ -899,11 +906,23 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 tc_fence_after();
                 {
                     const uint64_t dc = smem_desc_sw128(bC + kHalfBytes, 16, 1024), dh = smem_desc_sw128(bH, kHbufHead, 1024);
-#pragma unroll 1
+#pragma unroll
+                    for (uint32_t ks = 0; ks < 4; ++ks)
+                        mma_ss(tmem + ycol, dc + ks * 2, dh + ks * 128, kIdY, 1);
+                }
+                // ---- Y[b] += C h_lo^T: the low bf16 part of the fp32 state, all n ----
+                if (!(ok = wait_bar(sm, &sm.hlo_ready, kc & 1, status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (uint32_t j = 0; j < 2; ++j) {
+                    const uint64_t dc = smem_desc_sw128(bC + j * kHalfBytes, 16, 1024);
+                    const uint64_t dh = smem_desc_sw128(smem_u32(sm.hlo[j]), kHbufHead, 1024);
+#pragma unroll
                     for (uint32_t ks = 0; ks < 4; ++ks)
                         mma_ss(tmem + ycol, dc + ks * 2, dh + ks * 128, kIdY, 1);
                 }
                 mma_commit(&sm.yinter_ready);
+                mma_commit(&sm.hlo_free);
                 mma_commit(&sm.empty[tC % kSlots]);
                 mma_commit(&sm.empty[tC % kSlots]);
                 // ---- Y[b] += S_h X_h ----
@@ -914,7 +933,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 tc_fence_after();
                 {
                     const uint64_t dx = smem_desc_sw128(bX, 1024, 1024);
-#pragma unroll 1
+#pragma unroll
                     for (uint32_t i = 0; i < 16; ++i) {
                         const uint32_t hh = i >> 3, ks = i & 7;
                         const uint32_t acol = kColG + 16 * ks + 8 * hh;     // S_h, tokens 16ks..16ks+15
@@ -1037,7 +1056,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                     tc_fence_after();
                     const uint64_t db = smem_desc_sw128(smem_u32(sm.slot[tB % kSlots]), kHalfBytes, 1024);
                     const uint64_t dw = smem_desc_sw128(smem_u32(sm.xw[0]), kHalfBytes, 1024);
-#pragma unroll 1
+#pragma unroll
                     for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
                     mma_commit(&sm.xbuf_free);
                 }
@@ -1070,7 +1089,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 tc_fence_after();
                 const uint64_t db = smem_desc_sw128(smem_u32(sm.slot[tB % kSlots]), kHalfBytes, 1024);
                 const uint64_t dw = smem_desc_sw128(smem_u32(sm.xw[0]), kHalfBytes, 1024);
-#pragma unroll 1
+#pragma unroll
                 for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tmem + kColH, db + ks * 128, dw + ks * 128, kIdH, 1);
                 mma_commit(&sm.state_done);
                 mma_commit(&sm.xbuf_free);
@@ -1320,21 +1339,36 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 }
                 tmem_wait_st();
             }
-            uint32_t packed[64];                  // bf16 copy of this lane's 128 state values
+            uint32_t packed[64];                  // bf16 copy (hi part) of this lane's 128 state values
             // per head: the state entering the block is hs * eprev; renormalised
-            // accumulators hold exp(dlt) h instead
+            // accumulators hold exp(dlt) h instead.  h = hi + lo with both parts
+            // bf16: hi stays in registers for the two half-n copies below, lo goes
+            // straight to its own buffer (row n of each head), once the previous
+            // block's C h_lo^T has read it.
             const float2 ep0 = make_float2(ar.eprev[0], ar.eprev[0]), ep1 = make_float2(ar.eprev[1], ar.eprev[1]);
             const bool rn0 = ar.renorm[0] != 0, rn1 = ar.renorm[1] != 0;
+            if (kc > 0 && !(ok = warp_wait(sm, &sm.hlo_free, (kc - 1) & 1, status))) break;
+            uint8_t *lorow = sm.hlo[n >> 6] + hrow * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {                 // 16 columns at a time
                 uint32_t r[16];
                 tmem_ld16(tmem + lane_off + kColH + 16 * j, r);
                 tmem_wait_ld();
                 const float2 ep = (j >> 2) ? ep1 : ep0;
+                uint32_t lo[8];
 #pragma unroll
-                for (int i2 = 0; i2 < 8; ++i2)       // h entering the block (eprev = 1 at an item's first block)
-                    packed[j * 8 + i2] = pack2(__fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep));
+                for (int i2 = 0; i2 < 8; ++i2) {     // h entering the block (eprev = 1 at an item's first block)
+                    const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ep);
+                    const uint32_t hi = pack2(h);
+                    packed[j * 8 + i2] = hi;
+                    lo[i2] = pack2(__fadd2_rn(h, make_float2(-bf16_lo(hi), -bf16_hi(hi))));
+                }
+                uint8_t *lp = lorow + (j >> 2) * kHbufHead;
+                const int cc = 2 * (j & 3);
+                *reinterpret_cast<uint4 *>(lp + ((cc ^ (hrow & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(lp + (((cc + 1) ^ (hrow & 7)) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
             }
+            fence_proxy_async_smem();
             if (rn0 || rn1) {
                 // renormalise the accumulator to exp(dlt) h (rare: the block's exponents
                 // left the range of the running scale)
@@ -1363,6 +1397,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (lane == 0) {
                 mbar_arrive(&sm.state_ok);
                 mbar_arrive(&sm.arr_free[ab]);
+                mbar_arrive(&sm.hlo_ready);
             }
             // ---- bf16 copy of h for C h^T ----
             if (first_half) {
