@@ -10,11 +10,17 @@ is flushed (256 MiB write) between timed steps and each step is timed with
 CUDA events on the launching stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--no-per-config]
+
+The headline workload defaults to ``varlen_prefill`` (32 packed sequences,
+about 62 K tokens, the largest configuration); the same run then times every
+other named configuration (dense prefill, both continued prefills, MTP, the
+tiny fp32 case) with the same method and reports each under ``per_config``.
 
 Under torchrun every rank runs its own copy of the workload (the scan shards
 by sequence and head with no exchange: weak scaling, no collective on the
-data path); value = tokens of all ranks / max-over-ranks time.
+data path); value = tokens of all ranks / max-over-ranks time.  ``--gpus``
+must equal the launcher's WORLD_SIZE.
 """
 from __future__ import annotations
 
@@ -31,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSD scan tokens/s (1 GB300) and % of roofline; vs CPU oracle tokens/s"
-DEFAULT_WORKLOAD = "dense_prefill"
+DEFAULT_WORKLOAD = "varlen_prefill"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -206,60 +212,65 @@ def whole_job_rate(units_per_rank, world, ms_per_step_max):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, rank, world, local_rank):
+PER_CONFIG = ("dense_prefill", "varlen_prefill", "continued_a", "continued_b", "mtp", "tiny")
+
+
+def _dev_tensor(a, dtype_name, dev):
     import numpy as np
     import torch
-    import state_space_model_varlen_gb300 as ssd
-    from state_space_model_varlen_gb300 import workloads as W
+    if dtype_name == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    ssd.load()
-    p = W.workload(args.workload)
-    T, H, P, N = p.total_tokens, p.nheads, p.headdim, p.dstate
 
-    def dev_t(a, dtype_name):
-        if dtype_name == "bf16":
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+class _Resident:
+    """One workload's inputs and outputs resident on the device, with the
+    C-ABI parameter block that points at them."""
 
-    x = dev_t(p.x, p.io_dtype)
-    B = dev_t(p.B, p.io_dtype)
-    C = dev_t(p.C, p.io_dtype)
-    dt = torch.from_numpy(p.dt).to(dev)
-    A = torch.from_numpy(p.A).to(dev)
-    D = None if p.D is None else torch.from_numpy(p.D).to(dev)
-    bias = None if p.dt_bias is None else torch.from_numpy(p.dt_bias).to(dev)
-    cu = torch.from_numpy(p.cu_seqlens).to(dev)
-    slots = torch.from_numpy(p.slot_idx).to(dev)
-    has_init = None if p.has_init is None else torch.from_numpy(p.has_init).to(dev)
-    cache = dev_t(p.cache, p.state_dtype)
-    y = torch.empty_like(x)
-    st_t = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.state_dtype]
-    inter = torch.empty((T, H, P, N), dtype=st_t, device=dev) if p.want_intermediate else None
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    params = ssd.make_params(x, dt, A, B, C, cu, dt_bias=bias, D=D, state_cache=cache,
-                             slot_idx=slots, has_init=has_init, write_final=p.write_final,
-                             out_y=y, out_intermediate=inter, dt_softplus=p.dt_softplus,
-                             chunk_size=p.chunk_size, max_seqlen=p.max_seqlen,
-                             device_status=status)
-    need = ssd.workspace_size(params)
-    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    params.workspace, params.workspace_bytes = ws.data_ptr(), ws.numel()
-    launches = ssd.num_launches(params)
-    path = ssd.kernel_path(params)
-    stream = torch.cuda.current_stream(dev)
+    def __init__(self, ssd, p, dev):
+        import torch
+        self.p = p
+        T, H, P, N = p.total_tokens, p.nheads, p.headdim, p.dstate
+        self.x = _dev_tensor(p.x, p.io_dtype, dev)
+        self.B = _dev_tensor(p.B, p.io_dtype, dev)
+        self.C = _dev_tensor(p.C, p.io_dtype, dev)
+        self.dt = torch.from_numpy(p.dt).to(dev)
+        A = torch.from_numpy(p.A).to(dev)
+        D = None if p.D is None else torch.from_numpy(p.D).to(dev)
+        bias = None if p.dt_bias is None else torch.from_numpy(p.dt_bias).to(dev)
+        cu = torch.from_numpy(p.cu_seqlens).to(dev)
+        self.slots = torch.from_numpy(p.slot_idx).to(dev)
+        has_init = None if p.has_init is None else torch.from_numpy(p.has_init).to(dev)
+        self.cache = _dev_tensor(p.cache, p.state_dtype, dev)
+        self.y = torch.empty_like(self.x)
+        st_t = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.state_dtype]
+        self.inter = torch.empty((T, H, P, N), dtype=st_t, device=dev) if p.want_intermediate else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._keep = (A, D, bias, cu, has_init)
+        self.params = ssd.make_params(
+            self.x, self.dt, A, self.B, self.C, cu, dt_bias=bias, D=D, state_cache=self.cache,
+            slot_idx=self.slots, has_init=has_init, write_final=p.write_final, out_y=self.y,
+            out_intermediate=self.inter, dt_softplus=p.dt_softplus, chunk_size=p.chunk_size,
+            max_seqlen=p.max_seqlen, device_status=self.status)
+        need = ssd.workspace_size(self.params)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.params.workspace, self.params.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
+        self.launches = ssd.num_launches(self.params)
+        self.path = ssd.kernel_path(self.params)
+
+
+def _time_device(ssd, r, stream, steps, warmup, flush, local_rank, world):
+    """Device time of ``steps`` calls (CUDA events on the launching stream, L2
+    flushed between calls), with the SM clocks sampled meanwhile."""
+    import torch
     sptr = stream.cuda_stream
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    for _ in range(args.warmup):
-        ssd.call(params, sptr)
+    for _ in range(warmup):
+        ssd.call(r.params, sptr)
     torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError("device status %d after warm-up" % int(status.item()))
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if int(r.status.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(r.status.item()))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -267,20 +278,49 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.25)                      # let the sampler take its first reading
     t_wall = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         flush.fill_(i)                    # L2 flush (outside the events)
         starts[i].record(stream)
-        ssd.call(params, sptr)
+        ssd.call(r.params, sptr)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
+    total_ms = float(sum(s.elapsed_time(e) for s, e in zip(starts, ends)))
+    return total_ms, clocks, wall
+
+
+def _roofline_entry(p, ms_per_step):
+    hbm_peak, _, peak_kind = _peaks()
+    b = algorithmic_bytes(p)
+    achieved = b / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "peak_kind": peak_kind + " (burst copy)",
+            "algorithmic_bytes_per_launch": b}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import state_space_model_varlen_gb300 as ssd
+    from state_space_model_varlen_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ssd.load()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    p = W.workload(args.workload)
+    T = p.total_tokens
+    r = _Resident(ssd, p, dev)
+    launches, path = r.launches, r.path
+    total_ms, clocks, wall = _time_device(ssd, r, stream, args.steps, args.warmup, flush,
+                                          local_rank, world)
 
     # ---- end to end through the C ABI with host buffers --------------------
+    x, B, C, dt, y, cache, inter, slots = r.x, r.B, r.C, r.dt, r.y, r.cache, r.inter, r.slots
+    params, sptr = r.params, stream.cuda_stream
     pin = lambda t: t.cpu().pin_memory()
     hx, hB, hC, hdt = pin(x), pin(B), pin(C), pin(dt)
     hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
@@ -318,19 +358,55 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    del r, hx, hB, hC, hdt, hy, x, B, C, dt, y, cache, inter, params
+    torch.cuda.empty_cache()
+
+    # ---- every other config of the task, same method ------------------------
+    per_config = {}
+    if not args.no_per_config:
+        pc_steps = max(3, min(args.steps, args.per_config_steps))
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            q = W.workload(name)
+            rq = _Resident(ssd, q, dev)
+            ms, ck, _ = _time_device(ssd, rq, stream, pc_steps, args.warmup, flush, local_rank, world)
+            per_config[name] = {"ms": ms, "steps": pc_steps, "clocks": ck, "problem": q,
+                                "launches": rq.launches, "path": rq.path}
+            del rq
+            torch.cuda.empty_cache()
 
     # ---- max over ranks ------------------------------------------------------
-    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
+    names = sorted(per_config)
+    vals = max_over_ranks([total_ms, e2e_ms] + [per_config[n]["ms"] for n in names], dev)
+    total_ms, e2e_ms = vals[0], vals[1]
+    for n, v in zip(names, vals[2:]):
+        per_config[n]["ms"] = v
     if rank != 0:
         return None
 
     ms_per_step = total_ms / args.steps
     tokens_all = T * world
     value = whole_job_rate(T, world, ms_per_step)
-    hbm_peak, tc_peak, peak_kind = _peaks()
+    _, tc_peak, _ = _peaks()
     bytes_per_call = algorithmic_bytes(p)
-    achieved_gbs = bytes_per_call / (ms_per_step / 1e3) / 1e9
-    traffic = _traffic_per_launch(args.workload)
+    roof = _roofline_entry(p, ms_per_step)
+    roof.update({
+        "traffic": _traffic_per_launch(args.workload),
+        "algorithmic_flops_per_launch": algorithmic_flops(p),
+        "tensor_time_at_peak_us": algorithmic_flops(p) / (tc_peak * 1e12) * 1e6,
+        "hbm_time_at_peak_us": bytes_per_call / (roof["peak"] * 1e9) * 1e6,
+        "note": "achieved = algorithmic bytes / device time of the whole call "
+                "(%d launch(es)); a lower bound for the dominant kernel" % launches,
+    })
+    pc_out = {}
+    for n in names:
+        e = per_config[n]
+        q, ms = e["problem"], e["ms"] / e["steps"]
+        pc_out[n] = {"value": whole_job_rate(q.total_tokens, world, ms), "unit": "tokens/s",
+                     "ms_per_step": ms, "steps": e["steps"], "kernel_path": e["path"],
+                     "launches_per_call": e["launches"], "tokens": q.total_tokens,
+                     "roofline": _roofline_entry(q, ms), "clocks": e["clocks"]}
     line = {
         "metric": METRIC,
         "value": value,
@@ -345,28 +421,15 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16" if path == "chunked_tc" else "f32",
         "data": "synthetic (seeded, distributions of the workload recipe)",
         "config": {
-            "workload": args.workload, "tokens": T, "seqs": p.num_seqs, "nheads": H,
-            "headdim": P, "dstate": N, "ngroups": p.ngroups, "chunk_size": p.chunk_size,
-            "io_dtype": p.io_dtype, "state_dtype": p.state_dtype, "kernel_path": path,
+            "workload": args.workload, "tokens": T, "seqs": p.num_seqs, "nheads": p.nheads,
+            "headdim": p.headdim, "dstate": p.dstate, "ngroups": p.ngroups,
+            "chunk_size": p.chunk_size, "io_dtype": p.io_dtype, "state_dtype": p.state_dtype,
+            "kernel_path": path,
             "parallelism": "replicas x%d (independent batches, no collective)" % world,
             "l2": "flushed between timed steps (256 MiB write); working set %.0f MB"
                   % (bytes_per_call / 1e6),
         },
-        "roofline": {
-            "bound": "hbm",
-            "achieved": achieved_gbs,
-            "peak": hbm_peak,
-            "unit": "GB/s",
-            "frac": achieved_gbs / hbm_peak,
-            "traffic": traffic,
-            "peak_kind": peak_kind + " (burst copy)",
-            "algorithmic_bytes_per_launch": bytes_per_call,
-            "algorithmic_flops_per_launch": algorithmic_flops(p),
-            "tensor_time_at_peak_us": algorithmic_flops(p) / (tc_peak * 1e12) * 1e6,
-            "hbm_time_at_peak_us": bytes_per_call / (hbm_peak * 1e9) * 1e6,
-            "note": "achieved = algorithmic bytes / device time of the whole call "
-                    "(%d launch(es)); a lower bound for the dominant kernel" % launches,
-        },
+        "roofline": roof,
         "e2e": {
             "value": tokens_all / (e2e_ms / 1e3),
             "unit": "tokens/s",
@@ -376,6 +439,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
+        "per_config": pc_out,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
@@ -466,12 +530,18 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload, not the other configs")
+    ap.add_argument("--per-config-steps", type=int, default=20)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit("--gpus %d but WORLD_SIZE=%d: launch N>1 under torch.distributed.run "
+                         "with --nproc-per-node N" % (args.gpus, world))
     if args.impl == "reference":
         line = run_reference(args, rank)
         if line is not None:
