@@ -23,6 +23,13 @@
  *   y uses the state after token t's update.  The chunked form is an exact
  *   regrouping of this recurrence, so the oracle does no chunking at all.
  *
+ *   Checkpoint (per-chunk) states: prefills that store Mamba checkpoints need
+ *   the state at every chunk boundary ("Prefills that store Mamba checkpoints
+ *   need every chunk state", vLLM PR #61501 "Details").  Read plainly: with
+ *   chunk size L, row cu_chunks[s] + c of h_chunk is the state after token
+ *   min((c + 1) L, len_s) - 1 of sequence s, for c = 0 .. ceil(len_s / L) - 1;
+ *   the last row of a sequence is its final state.
+ *
  * Everything is fp64 and walks the tokens in order; independent (sequence,
  * head) chains may run on different threads, which does not change any
  * arithmetic.
@@ -54,7 +61,9 @@ int ssd_oracle_threads(void) {
  *   x [T,H,P], dt [T,H], dt_bias [H] or NULL, A [H], B/C [T,G,N], D [H] or NULL,
  *   cu_seqlens int64 [S+1], h_init [S,H,P,N] or NULL (zero initial state),
  *   y [T,H,P] (written for heads in [head_begin, head_end)),
- *   h_final [S,H,P,N] or NULL, h_inter [T,H,P,N] or NULL.
+ *   h_final [S,H,P,N] or NULL, h_inter [T,H,P,N] or NULL,
+ *   chunk_size L, cu_chunks int64 [S+1] and h_chunk [cu_chunks[S],H,P,N], or
+ *   h_chunk NULL (then L and cu_chunks are not read).
  * Returns 0, or -1 for inconsistent sizes.
  */
 int ssd_oracle_scan(int64_t total_tokens, int32_t num_seqs, int32_t nheads,
@@ -64,7 +73,8 @@ int ssd_oracle_scan(int64_t total_tokens, int32_t num_seqs, int32_t nheads,
                     int32_t dt_softplus, const double *A, const double *B,
                     const double *C, const double *D, const int64_t *cu_seqlens,
                     const double *h_init, double *y, double *h_final,
-                    double *h_inter, int32_t num_threads) {
+                    double *h_inter, int32_t num_threads, int32_t chunk_size,
+                    const int64_t *cu_chunks, double *h_chunk) {
     const int64_t T = total_tokens;
     const int S = num_seqs, H = nheads, P = headdim, N = dstate, G = ngroups;
     if (S < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return -1;
@@ -72,6 +82,13 @@ int ssd_oracle_scan(int64_t total_tokens, int32_t num_seqs, int32_t nheads,
     if (S > 0 && (cu_seqlens[0] != 0 || cu_seqlens[S] != T)) return -1;
     for (int s = 0; s < S; ++s)
         if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+    if (h_chunk) {
+        if (chunk_size <= 0 || cu_chunks[0] != 0) return -1;
+        for (int s = 0; s < S; ++s) {
+            const int64_t len = cu_seqlens[s + 1] - cu_seqlens[s];
+            if (cu_chunks[s + 1] - cu_chunks[s] != (len + chunk_size - 1) / chunk_size) return -1;
+        }
+    }
     const int heads_per_group = H / G;
     const int nh = head_end - head_begin;
     const int64_t pairs = (int64_t)S * nh;
@@ -108,6 +125,12 @@ int ssd_oracle_scan(int64_t total_tokens, int32_t num_seqs, int32_t nheads,
             if (h_inter)
                 memcpy(h_inter + (t * H + h) * (int64_t)P * N, state,
                        sizeof(double) * (size_t)P * N);
+            const int64_t pos = t - cu_seqlens[s];          /* token index within the sequence */
+            if (h_chunk && ((pos + 1) % chunk_size == 0 || t == cu_seqlens[s + 1] - 1)) {
+                const int64_t row = cu_chunks[s] + pos / chunk_size;
+                memcpy(h_chunk + (row * H + h) * (int64_t)P * N, state,
+                       sizeof(double) * (size_t)P * N);
+            }
         }
         if (h_final)
             memcpy(h_final + ((int64_t)s * H + h) * P * N, state,

@@ -98,6 +98,10 @@ class Problem:
     has_init: Optional[np.ndarray]  # uint8 [S]
     write_final: int
     want_intermediate: int
+    # optional parts of the call (defaults: the plain scan)
+    final_slot_idx: Optional[np.ndarray] = None   # int32 [S]: where final states go (None: slot_idx)
+    want_chunk_states: int = 0                    # also return the state at every chunk boundary
+    sr_seed: Optional[int] = None                 # fp16 cache writes with stochastic rounding
 
     @property
     def num_seqs(self) -> int:
@@ -118,6 +122,23 @@ class Problem:
     @property
     def max_seqlen(self) -> int:
         return int(self.seqlens.max()) if self.num_seqs else 0
+
+    @property
+    def final_slots(self) -> np.ndarray:
+        return self.slot_idx if self.final_slot_idx is None else self.final_slot_idx
+
+    @property
+    def cu_chunks(self) -> np.ndarray:
+        return chunk_offsets(self.seqlens, self.chunk_size)
+
+
+def chunk_offsets(seqlens, chunk_size) -> np.ndarray:
+    """int32 [S+1]: first checkpoint row of each sequence, ceil(len / chunk_size)
+    rows per sequence (the layout of the per-chunk state output)."""
+    lens = np.asarray(seqlens, dtype=np.int64)
+    out = np.zeros(lens.shape[0] + 1, dtype=np.int64)
+    out[1:] = np.cumsum((lens + chunk_size - 1) // chunk_size)
+    return out.astype(np.int32)
 
 
 def make_problem(seqlens, *, nheads, headdim, dstate, ngroups=1, chunk_size=128,
@@ -222,5 +243,6 @@ def select_sequences(p: Problem, seqs) -> Problem:
     return dataclasses.replace(
         p, cu_seqlens=ncu.astype(np.int32), x=p.x[rows], dt=p.dt[rows], B=p.B[rows], C=p.C[rows],
         slot_idx=p.slot_idx[seqs].copy(),
+        final_slot_idx=None if p.final_slot_idx is None else p.final_slot_idx[seqs].copy(),
         has_init=None if p.has_init is None else p.has_init[seqs].copy(),
         cache=p.cache.copy())

@@ -289,3 +289,43 @@ def test_planted_slip_is_caught_by_hand_example(slip):
     np.testing.assert_allclose(y_ok.reshape(-1), g["y"], atol=1e-12)
     y_bad, _ = _python_recurrence(*args, slip=slip)
     assert np.max(np.abs(y_bad.reshape(-1) - g["y"])) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# the head slice and the no-softplus-with-bias activation
+# --------------------------------------------------------------------------
+def test_head_slice_equals_those_heads_of_a_full_run():
+    """``heads=(h0, h1)`` (used by every sampled full-size parity test) computes
+    exactly those heads of the full run and leaves the other heads' outputs at
+    zero; the full run itself is pinned by the dual form above."""
+    p = W.make_problem([9, 0, 23, 5], nheads=8, headdim=3, dstate=5, ngroups=4, io_dtype="f32",
+                       num_slots=6, has_init=[1, 0, 0, 1], seed=27)
+    full = oracle.ssd_scan_reference(p)
+    for h0, h1 in ((0, 8), (2, 5), (7, 8), (3, 3)):
+        part = oracle.ssd_scan_reference(p, heads=(h0, h1))
+        np.testing.assert_array_equal(part["y"][:, h0:h1], full["y"][:, h0:h1])
+        np.testing.assert_array_equal(part["final"][:, h0:h1], full["final"][:, h0:h1])
+        others = [h for h in range(8) if not h0 <= h < h1]
+        assert not np.any(part["y"][:, others])
+        for s in range(p.num_seqs):
+            slot = int(p.slot_idx[s])
+            np.testing.assert_array_equal(part["cache"][slot, h0:h1], full["cache"][slot, h0:h1])
+            np.testing.assert_array_equal(part["cache"][slot, others], p.cache[slot, others])
+
+
+def test_bias_without_softplus_matches_dual_form():
+    """dt_softplus = 0 with a bias: dt' = dt + dt_bias, checked against the
+    independent dual form with its softplus switched off."""
+    rng = np.random.default_rng(28)
+    L, H, P, N = 26, 3, 4, 5
+    x, B, C = _rand(rng, L, H, P), _rand(rng, L, 1, N), _rand(rng, L, 1, N)
+    dt = rng.uniform(0.01, 0.2, (L, H))
+    bias = rng.uniform(0.0, 0.05, H)
+    A, D = -rng.uniform(1, 8, H), _rand(rng, H)
+    h0 = _rand(rng, 1, H, P, N)
+    y, hf, _ = oracle.scan(x, dt, A, B, C, [0, L], dt_bias=bias, dt_softplus=False, D=D, h_init=h0)
+    for h in range(H):
+        yd, hd = dual_form_head(x[:, h], dt[:, h], A[h], B[:, 0], C[:, 0], D=D[h], h0=h0[0, h],
+                                dt_bias=bias[h], softplus=False)
+        np.testing.assert_allclose(y[:, h], yd, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(hf[0, h], hd, rtol=1e-11, atol=1e-12)
