@@ -62,6 +62,24 @@ def algorithmic_bytes(p) -> int:
     return int(b)
 
 
+def replay_bytes(p, ring) -> int:
+    """Algorithmic bytes of one ReplaySSM verification step: checkpoints read,
+    pending ring inputs read, window inputs read and y written, window inputs
+    appended to the ring, and the checkpoints of requests that fold written."""
+    io = 2 if p.io_dtype == "bf16" else 4
+    st = 4 if p.state_dtype == "f32" else 2
+    H, P, N, G, S = p.nheads, p.headdim, p.dstate, p.ngroups, p.num_seqs
+    tok_in = H * P * io + H * 4 + G * N * io          # one token's x, dt, B
+    state = H * P * N * st
+    K = p.seqlens
+    b = S * state                                       # checkpoints
+    b += int(sum(int(c) for c in ring["count"])) * tok_in
+    b += p.total_tokens * (tok_in + G * N * io + H * P * io)   # window x, dt, B, C in; y out
+    b += p.total_tokens * tok_in                        # appended to the ring
+    b += int(sum(1 for c, k in zip(ring["count"], K) if c + k > ring["window"])) * state
+    return int(b)
+
+
 def algorithmic_flops(p) -> int:
     """Chunked-SSD contraction work with causal halves counted (per chunk and
     head: 2lNP chunk state + 2lNP C.h_prev + P l(l+1) masked scores.X; per
@@ -212,7 +230,8 @@ def whole_job_rate(units_per_rank, world, ms_per_step_max):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-PER_CONFIG = ("dense_prefill", "varlen_prefill", "continued_a", "continued_b", "mtp", "tiny")
+PER_CONFIG = ("dense_prefill", "varlen_prefill", "continued_a", "continued_b", "mtp", "mtp_replay",
+              "tiny")
 
 
 def _dev_tensor(a, dtype_name, dev):
@@ -259,13 +278,47 @@ class _Resident:
         self.path = ssd.kernel_path(self.params)
 
 
+class _ResidentReplay(_Resident):
+    """The MTP windows plus rings on the device, verified with ssd_replay_mtp."""
+
+    def __init__(self, ssd, p, dev):
+        import torch
+        from state_space_model_varlen_gb300 import workloads as W
+        super().__init__(ssd, p, dev)
+        self.ring = W.replay_ring(p, seed=40)
+        self.rx = _dev_tensor(self.ring["x"], p.io_dtype, dev)
+        self.rdt = torch.from_numpy(self.ring["dt"]).to(dev)
+        self.rB = _dev_tensor(self.ring["B"], p.io_dtype, dev)
+        self.rstart = torch.from_numpy(self.ring["start"]).to(dev)
+        self.rcount = torch.from_numpy(self.ring["count"]).to(dev)
+        self.rstart_out = torch.empty_like(self.rstart)
+        self.rcount_out = torch.empty_like(self.rcount)
+        self.params.write_final = 0
+        self.params.has_init = None
+        self.replay = ssd.make_replay_params(self.params, self.rx, self.rdt, self.rB,
+                                             self.ring["window"], self.rstart, self.rcount,
+                                             self.rstart_out, self.rcount_out)
+        self.launches, self.path = 1, "replay"
+        self._ssd = ssd
+
+    def call(self, sptr):
+        self._ssd.call_replay(self.replay, sptr)
+
+
+def _call(ssd, r, sptr):
+    if isinstance(r, _ResidentReplay):
+        r.call(sptr)
+    else:
+        ssd.call(r.params, sptr)
+
+
 def _time_device(ssd, r, stream, steps, warmup, flush, local_rank, world):
     """Device time of ``steps`` calls (CUDA events on the launching stream, L2
     flushed between calls), with the SM clocks sampled meanwhile."""
     import torch
     sptr = stream.cuda_stream
     for _ in range(warmup):
-        ssd.call(r.params, sptr)
+        _call(ssd, r, sptr)
     torch.cuda.synchronize()
     if int(r.status.item()) != 0:
         raise RuntimeError("device status %d after warm-up" % int(r.status.item()))
@@ -281,7 +334,7 @@ def _time_device(ssd, r, stream, steps, warmup, flush, local_rank, world):
     for i in range(steps):
         flush.fill_(i)                    # L2 flush (outside the events)
         starts[i].record(stream)
-        ssd.call(r.params, sptr)
+        _call(ssd, r, sptr)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
@@ -292,9 +345,9 @@ def _time_device(ssd, r, stream, steps, warmup, flush, local_rank, world):
     return total_ms, clocks, wall
 
 
-def _roofline_entry(p, ms_per_step):
+def _roofline_entry(p, ms_per_step, b=None):
     hbm_peak, _, peak_kind = _peaks()
-    b = algorithmic_bytes(p)
+    b = algorithmic_bytes(p) if b is None else b
     achieved = b / (ms_per_step / 1e3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved / hbm_peak, "peak_kind": peak_kind + " (burst copy)",
@@ -369,10 +422,11 @@ def run_ours(args, rank, world, local_rank):
             if name == args.workload:
                 continue
             q = W.workload(name)
-            rq = _Resident(ssd, q, dev)
+            rq = _ResidentReplay(ssd, q, dev) if name == "mtp_replay" else _Resident(ssd, q, dev)
             ms, ck, _ = _time_device(ssd, rq, stream, pc_steps, args.warmup, flush, local_rank, world)
             per_config[name] = {"ms": ms, "steps": pc_steps, "clocks": ck, "problem": q,
-                                "launches": rq.launches, "path": rq.path}
+                                "launches": rq.launches, "path": rq.path,
+                                "bytes": replay_bytes(q, rq.ring) if name == "mtp_replay" else None}
             del rq
             torch.cuda.empty_cache()
 
@@ -406,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
         pc_out[n] = {"value": whole_job_rate(q.total_tokens, world, ms), "unit": "tokens/s",
                      "ms_per_step": ms, "steps": e["steps"], "kernel_path": e["path"],
                      "launches_per_call": e["launches"], "tokens": q.total_tokens,
-                     "roofline": _roofline_entry(q, ms), "clocks": e["clocks"]}
+                     "roofline": _roofline_entry(q, ms, e["bytes"]), "clocks": e["clocks"]}
     line = {
         "metric": METRIC,
         "value": value,

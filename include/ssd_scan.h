@@ -18,9 +18,16 @@
  *   h_{-1}   = has_init[s] ? state_cache[slot_idx[s], h] : 0   (fp32 math)
  *   h_t[p,n] = exp(dt'_t A[h]) h_{t-1}[p,n] + dt'_t x[t,h,p] B[t,g,n]
  *   y[t,h,p] = sum_n C[t,g,n] h_t[p,n] + D[h] x[t,h,p]          (D 0 if NULL)
- *   state_cache[slot_idx[s], h] = h_last   (write_final; rounded to nearest
- *                                           even in the cache dtype)
+ *   state_cache[final_slot[s], h] = h_last (write_final; final_slot = slot_idx
+ *                                           unless final_slot_idx is given;
+ *                                           rounded to nearest even in the
+ *                                           cache dtype, or stochastically, see
+ *                                           sr_seed)
  *   out_intermediate[t, h] = h_t           (if not NULL)
+ *   out_chunk_states[cu_chunks[s] + c, h] = h after token
+ *       min((c + 1) chunk_size, len_s) - 1 of sequence s  (if not NULL): the
+ *       state at every chunk boundary, which prefills that store Mamba
+ *       checkpoints need (vLLM PR #61501 "Details")
  *
  * Layouts (all dense, row-major, innermost index last):
  *   x, out_y         [T, H, P]            io_dtype (F32 or BF16)
@@ -30,9 +37,15 @@
  *   cu_seqlens       [S+1]                int32, device; cu[0] = 0, cu[S] = T,
  *                                         non-decreasing (empty sequences ok)
  *   state_cache      [num_slots, H, P, N] state_dtype (F32, BF16 or F16)
- *   slot_idx         [S]                  int32, device
+ *   slot_idx         [S]                  int32, device, entry s at
+ *                                         slot_idx[s * slot_idx_stride]
+ *   final_slot_idx   [S]                  int32, device, or NULL (= slot_idx)
  *   has_init         [S]                  uint8, device, or NULL (= all zero)
  *   out_intermediate [T, H, P, N]         state_dtype, or NULL
+ *   out_chunk_states [num_chunk_rows, H, P, N] state_dtype, or NULL
+ *   cu_chunks        [S+1]                int32, device: cu_chunks[0] = 0 and
+ *                                         cu_chunks[s+1] - cu_chunks[s] =
+ *                                         ceil(len_s / chunk_size)
  * All pointers except `workspace` may be any device-accessible pointer the
  * kernels can read; the library itself never dereferences them on the host.
  *
@@ -44,12 +57,22 @@
  * hand states to one another); where the context has fewer SMs than the
  * device, that launch falls back to running every sequence whole.
  *
- * Aliasing: state_cache is read (initial states) and written (final states)
- * in place; a sequence's final state goes into the slot its initial state
- * came from.  out_y and out_intermediate must not overlap any input.  Two
- * sequences that name the same slot with write_final = 1 give an undefined
- * result for that slot.  Slots not named by slot_idx are never read or
- * written.
+ * Aliasing and snapshot semantics: state_cache is read (initial states) and
+ * written (final states) in place; by default a sequence's final state goes
+ * into the slot its initial state came from, and final_slot_idx sends it
+ * elsewhere.  Every initial state is the slot's content from before the call,
+ * even when another sequence of the same call writes that slot (crossed or
+ * shared slots; vLLM PR #62922 "Details": multi-sequence calls keep snapshot
+ * semantics).  The library takes that snapshot itself: when has_init and
+ * write_final are set for more than one sequence, a pass before the scan
+ * copies every initial state that another sequence's final slot would
+ * overwrite into the workspace (counted by ssd_scan_varlen_workspace_size).
+ * A caller that knows no slot is both read by one sequence and written by
+ * another sets slots_disjoint = 1 to skip that pass.  Two sequences that
+ * write the same final slot leave one of the two final states there
+ * (unspecified which).  out_y, out_intermediate and out_chunk_states must not
+ * overlap any input.  Slots named neither by slot_idx nor final_slot_idx are
+ * never read or written.
  *
  * Errors: invalid arguments return an error status and launch nothing.
  * Metadata that can only be checked on the device (slot index outside
@@ -86,6 +109,12 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype;
 #define SSD_DEV_BAD_SEQLENS 2     /* cu_seqlens[s..s+1] not within [0, T]      */
 #define SSD_DEV_TIMEOUT 4         /* an internal wait of the chunked kernel ran
                                      out of time; its outputs are incomplete   */
+#define SSD_DEV_BAD_CHUNKS 8      /* cu_chunks does not match the sequence
+                                     lengths or num_chunk_rows: that
+                                     sequence's chunk states are not written  */
+#define SSD_DEV_BAD_RING 16       /* ssd_replay_mtp: ring_start / ring_count out
+                                     of range, or the window does not fit the
+                                     ring; that request is skipped             */
 
 typedef struct {
     int64_t total_tokens;       /* T                                          */
@@ -96,8 +125,9 @@ typedef struct {
     int32_t headdim;            /* P                                          */
     int32_t dstate;             /* N                                          */
     int32_t ngroups;            /* G, divides H                               */
-    int32_t chunk_size;         /* >= 1; the chunked kernel's result does not
-                                   depend on it beyond rounding               */
+    int32_t chunk_size;         /* >= 1: the spacing of out_chunk_states;
+                                   y and final states do not depend on it
+                                   beyond rounding                            */
     int32_t io_dtype;           /* ssd_dtype of x, B, C, out_y                */
     int32_t state_dtype;        /* ssd_dtype of state_cache, out_intermediate */
     int32_t dt_softplus;        /* 1: dt' = softplus(dt + dt_bias)            */
@@ -121,6 +151,29 @@ typedef struct {
     void *workspace;            /* device scratch, see workspace_size         */
     size_t workspace_bytes;
     int32_t *device_status;     /* device int32 or NULL                       */
+    /* ---- optional parts of a call: zero / NULL turns each off ---- */
+    void *out_chunk_states;     /* per-chunk states, see the layout above     */
+    const int32_t *cu_chunks;   /* required with out_chunk_states             */
+    int32_t num_chunk_rows;     /* rows of out_chunk_states                   */
+    int32_t slots_disjoint;     /* 1: no slot is read by one sequence and
+                                   written by another (no snapshot pass)      */
+    const int32_t *final_slot_idx;   /* see above                             */
+    int64_t slot_idx_stride;         /* elements between entries, 0 = 1       */
+    int64_t final_slot_idx_stride;   /* elements between entries, 0 = 1       */
+    const uint64_t *sr_seed;    /* device, or NULL.  With state_dtype F16,
+                                   final and chunk states are rounded
+                                   stochastically: element e (flat index in
+                                   its tensor) rounds away from zero with
+                                   probability f = (|v| - |lo|) / (|hi| - |lo|)
+                                   (lo, hi: the fp16 values around v toward
+                                   and away from zero), i.e. when f * 2^32 >
+                                   word (e & 3) of Philox4x32-10 with key
+                                   (seed, seed >> 32) and counter (e >> 2,
+                                   e >> 34, stream, 0); stream 0 for
+                                   state_cache, 1 for out_chunk_states (vLLM
+                                   PR #61501 "Details": the ReplaySSM Philox
+                                   seed, read from a device buffer).  Ignored
+                                   for other state dtypes.                    */
 } ssd_scan_params;
 
 /* Bytes of device workspace a call with these parameters needs (a function
@@ -149,7 +202,8 @@ int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params);
  * states, continuations of at most 3 tokens, other shapes) or "invalid". */
 const char *ssd_scan_varlen_path(const ssd_scan_params *params);
 
-/* Maximum number of sequences ssd_scan_varlen_noalloc accepts. */
+/* Maximum number of sequences ssd_scan_varlen_noalloc accepts on the
+ * tensor-core path. */
 #define SSD_NOALLOC_MAX_SEQS 65536
 
 /* The same scan as ssd_scan_varlen for callers that cannot allocate device
@@ -159,12 +213,18 @@ const char *ssd_scan_varlen_path(const ssd_scan_params *params);
  * tensors, or a latency-critical path that cannot afford cudaMalloc's
  * device-wide synchronisation.  Instead of params->workspace (ignored here)
  * the scratch comes from a fixed array in the library's device memory, so
- * the call itself allocates nothing and calls no allocating routine.
- *   - Limit: num_seqs <= SSD_NOALLOC_MAX_SEQS, else SSD_ERR_SCRATCH_LIMIT and
- *     nothing is enqueued.  Every GPU that loads the library keeps the
- *     array (256 KiB) until the process exits.
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ * the call allocates nothing and calls no allocating routine (the first call
+ * on a device may load the library's module, which places the array; callers
+ * that reserve all free memory should make one call before doing so).
+ *   - Limit: on the tensor-core path num_seqs <= SSD_NOALLOC_MAX_SEQS, else
+ *     SSD_ERR_SCRATCH_LIMIT and nothing is enqueued (the token-by-token path
+ *     uses no scratch).  Calls that need the snapshot of initial states
+ *     (several sequences with has_init and write_final, slots_disjoint = 0)
+ *     are rejected the same way: the array has no room for states.  Every GPU
+ *     that loads the library keeps the array (256 KiB) until the process exits.
+ *   - Each call looks up the array's device address with the call's device
+ *     current; the first lookup on a device may load the module, so make the
+ *     first call before any stream capture.
  *   - All calls share the array.  Calls whose kernels may overlap on the GPU
  *     (unordered streams) race on it; order them on one stream or use
  *     ssd_scan_varlen with separate workspaces.  Nothing in the array needs
@@ -172,13 +232,77 @@ const char *ssd_scan_varlen_path(const ssd_scan_params *params);
  *   - Every sequence runs whole on one CTA (the array has no room for the
  *     hand-over states), so for batches that ssd_scan_varlen cuts into
  *     segments the results agree with it within rounding, not bit for bit,
- *     and take longer.
+ *     and take longer.  ssd_scan_varlen_num_launches called with
+ *     workspace_bytes = 0 gives this entry point's launch count.
  * Everything else (arguments, aliasing, errors, results) is as for
  * ssd_scan_varlen. */
 ssd_status ssd_scan_varlen_noalloc(const ssd_scan_params *params, struct CUstream_st *stream);
 
+/* ReplaySSM-style multi-token verification (vLLM PR #52928 "Summary": each
+ * layer keeps a checkpoint and a ring of inputs; the accepted length advances
+ * a shared cursor before the next forward; the checkpoint is updated only
+ * when the next verification window would overflow the ring).  Instead of
+ * storing the state after every speculative token, request s keeps, in slot
+ * q = slot_idx[s]:
+ *   state_cache[q]          the checkpoint,
+ *   ring_x/ring_dt/ring_B[q] the raw inputs (x, dt before bias/softplus, B)
+ *                           of the accepted tokens since the checkpoint, at
+ *                           positions (ring_start[s] + j) mod ring_capacity,
+ *                           j < ring_count[s].
+ * One call, with the window tokens of every request packed by cu_seqlens:
+ *   1. h = checkpoint advanced through the ring_count[s] pending inputs;
+ *   2. if ring_count[s] + window length > ring_window, the checkpoint becomes
+ *      h (cache dtype; stochastic rounding as in ssd_scan_params.sr_seed);
+ *   3. y of every window token from h, exactly as ssd_scan_varlen computes it;
+ *   4. the window's raw inputs are written to the ring positions following
+ *      the pending ones;
+ *   5. ring_start_out[s] / ring_count_out[s] receive where the live part of
+ *      the ring now starts and how many entries precede the window (after a
+ *      fold: the window's position and 0; else ring_start[s], ring_count[s]).
+ *      After sampling, the caller sets ring_start = ring_start_out and
+ *      ring_count = ring_count_out + accepted tokens.
+ * Requirements: ring_capacity >= ring_window + every window length (the
+ * window then never overwrites a pending entry); 0 <= ring_count <=
+ * ring_window; distinct slots per call; the scan fields write_final,
+ * out_intermediate, out_chunk_states and final_slot_idx unused (0 / NULL);
+ * has_init ignored (the checkpoint is always read).  Violations found on the
+ * device set SSD_DEV_BAD_RING and skip the request.  Layouts (dense):
+ *   ring_x [num_slots, ring_capacity, H, P]  io_dtype
+ *   ring_dt [num_slots, ring_capacity, H]    float32
+ *   ring_B [num_slots, ring_capacity, G, N]  io_dtype
+ * One kernel launch; no workspace; nothing is allocated or synchronised. */
+typedef struct {
+    ssd_scan_params scan;       /* window tokens, layer parameters, checkpoints */
+    void *ring_x;
+    float *ring_dt;
+    void *ring_B;
+    int32_t ring_capacity;
+    int32_t ring_window;
+    const int32_t *ring_start;  /* device [S] */
+    const int32_t *ring_count;  /* device [S] */
+    int32_t *ring_start_out;    /* device [S], must not alias ring_start */
+    int32_t *ring_count_out;    /* device [S], must not alias ring_count */
+} ssd_replay_params;
+
+ssd_status ssd_replay_mtp(const ssd_replay_params *params, struct CUstream_st *stream);
+
 /* Static description of a status code. */
 const char *ssd_status_string(ssd_status status);
+
+/* Test hooks of the tensor-core kernel's failure detection, for tests only
+ * (process-wide; restore with (0, -1, 0)).  No page counterpart.
+ *   wait_cycles > 0: every internal wait gives up after that many clock cycles
+ *     instead of about two seconds, sets SSD_DEV_TIMEOUT and makes the CTA's
+ *     roles leave their loops (the CTA still waits for its own TMA loads and
+ *     MMAs and frees its tensor memory before it exits);
+ *   withhold_handover >= 0: the segment hand-over with that index (boundary x
+ *     head pairs + head pair, in the order the prep kernel numbers them) is
+ *     never published, so the segment waiting for it runs out of time: the
+ *     host-made fault of the failure-detection test;
+ *   force_unsegmented = 1: batches that would be cut into segments run every
+ *     sequence whole instead (the path taken when a cooperative launch is
+ *     refused). */
+void ssd_testing_set_hooks(int64_t wait_cycles, int32_t withhold_handover, int32_t force_unsegmented);
 
 #ifdef __cplusplus
 }

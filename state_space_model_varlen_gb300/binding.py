@@ -17,11 +17,13 @@ from . import _build
  SSD_ERR_SCRATCH_LIMIT) = range(6)
 SSD_NOALLOC_MAX_SEQS = 65536
 SSD_F32, SSD_BF16, SSD_F16 = 0, 1, 2
-SSD_DEV_BAD_SLOT, SSD_DEV_BAD_SEQLENS = 1, 2
+SSD_DEV_BAD_SLOT, SSD_DEV_BAD_SEQLENS, SSD_DEV_TIMEOUT = 1, 2, 4
+SSD_DEV_BAD_CHUNKS, SSD_DEV_BAD_RING = 8, 16
 
 # every exported entry point declared in include/ssd_scan.h
-EXPORTED = ("ssd_scan_varlen", "ssd_scan_varlen_workspace_size", "ssd_scan_varlen_num_launches",
-            "ssd_scan_varlen_path", "ssd_status_string", "ssd_scan_varlen_noalloc")
+EXPORTED = ("ssd_replay_mtp", "ssd_scan_varlen", "ssd_scan_varlen_noalloc",
+            "ssd_scan_varlen_num_launches", "ssd_scan_varlen_path",
+            "ssd_scan_varlen_workspace_size", "ssd_status_string", "ssd_testing_set_hooks")
 
 
 class ScanParams(ctypes.Structure):
@@ -57,6 +59,30 @@ class ScanParams(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("device_status", ctypes.c_void_p),
+        ("out_chunk_states", ctypes.c_void_p),
+        ("cu_chunks", ctypes.c_void_p),
+        ("num_chunk_rows", ctypes.c_int32),
+        ("slots_disjoint", ctypes.c_int32),
+        ("final_slot_idx", ctypes.c_void_p),
+        ("slot_idx_stride", ctypes.c_int64),
+        ("final_slot_idx_stride", ctypes.c_int64),
+        ("sr_seed", ctypes.c_void_p),
+    ]
+
+
+class ReplayParams(ctypes.Structure):
+    """Mirror of ``ssd_replay_params``."""
+    _fields_ = [
+        ("scan", ScanParams),
+        ("ring_x", ctypes.c_void_p),
+        ("ring_dt", ctypes.c_void_p),
+        ("ring_B", ctypes.c_void_p),
+        ("ring_capacity", ctypes.c_int32),
+        ("ring_window", ctypes.c_int32),
+        ("ring_start", ctypes.c_void_p),
+        ("ring_count", ctypes.c_void_p),
+        ("ring_start_out", ctypes.c_void_p),
+        ("ring_count_out", ctypes.c_void_p),
     ]
 
 
@@ -90,6 +116,10 @@ def load(build_if_missing: bool = True):
             lib.ssd_scan_varlen_path.argtypes = [P]
             lib.ssd_scan_varlen_noalloc.restype = ctypes.c_int
             lib.ssd_scan_varlen_noalloc.argtypes = [P, ctypes.c_void_p]
+            lib.ssd_testing_set_hooks.restype = None
+            lib.ssd_testing_set_hooks.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+            lib.ssd_replay_mtp.restype = ctypes.c_int
+            lib.ssd_replay_mtp.argtypes = [ctypes.POINTER(ReplayParams), ctypes.c_void_p]
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -132,11 +162,27 @@ def _ptr(t, dtype=None):
     return t.data_ptr()
 
 
+def _index_ptr(t):
+    """A 1-D int32 index tensor, possibly a strided view (a block-table column):
+    (pointer, stride in elements)."""
+    torch = _torch()
+    if t is None:
+        return None, 0
+    if t.dtype != torch.int32 or t.dim() != 1:
+        raise TypeError("slot indices must be a 1-D int32 tensor")
+    return t.data_ptr(), int(t.stride(0))
+
+
 def make_params(x, dt, A, B, C, cu_seqlens, *, dt_bias=None, D=None, state_cache=None,
                 slot_idx=None, has_init=None, write_final=True, out_y=None,
                 out_intermediate=None, dt_softplus=True, chunk_size=128, max_seqlen=0,
-                workspace=None, device_status=None) -> ScanParams:
-    """Fill ``ssd_scan_params`` from torch tensors (no copies, no device reads)."""
+                workspace=None, device_status=None, final_slot_idx=None,
+                out_chunk_states=None, cu_chunks=None, sr_seed=None,
+                slots_disjoint=False) -> ScanParams:
+    """Fill ``ssd_scan_params`` from torch tensors (no copies, no device reads).
+
+    ``slot_idx`` / ``final_slot_idx`` may be strided int32 views; ``sr_seed``
+    is a one-element int64 device tensor (its bits are the 64-bit seed)."""
     torch = _torch()
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
@@ -161,7 +207,20 @@ def make_params(x, dt, A, B, C, cu_seqlens, *, dt_bias=None, D=None, state_cache
     p.dt_bias, p.D = _ptr(dt_bias, torch.float32), _ptr(D, torch.float32)
     p.cu_seqlens = _ptr(cu_seqlens, torch.int32)
     p.state_cache = _ptr(state_cache)
-    p.slot_idx = _ptr(slot_idx, torch.int32)
+    p.slot_idx, p.slot_idx_stride = _index_ptr(slot_idx)
+    p.final_slot_idx, p.final_slot_idx_stride = _index_ptr(final_slot_idx)
+    if out_chunk_states is not None:
+        if cu_chunks is None:
+            raise ValueError("out_chunk_states needs cu_chunks")
+        if state_cache is not None and out_chunk_states.dtype != state_cache.dtype:
+            raise TypeError("out_chunk_states must have the state cache dtype")
+        p.out_chunk_states = _ptr(out_chunk_states)
+        p.num_chunk_rows = out_chunk_states.shape[0]
+    p.cu_chunks = _ptr(cu_chunks, torch.int32)
+    if sr_seed is not None and sr_seed.dtype not in (torch.int64, torch.uint64):
+        raise TypeError("sr_seed must be a 64-bit integer tensor")
+    p.sr_seed = None if sr_seed is None else sr_seed.data_ptr()
+    p.slots_disjoint = int(bool(slots_disjoint))
     if has_init is not None and has_init.dtype == torch.bool:
         has_init = has_init.view(torch.uint8)
     p.has_init = _ptr(has_init, torch.uint8)
@@ -189,6 +248,35 @@ def call(params: ScanParams, stream_ptr: int = 0) -> None:
     rc = load().ssd_scan_varlen(ctypes.byref(params), ctypes.c_void_p(stream_ptr or None))
     if rc != SSD_OK:
         raise SSDError(rc)
+
+
+def make_replay_params(scan: ScanParams, ring_x, ring_dt, ring_B, ring_window, ring_start,
+                       ring_count, ring_start_out, ring_count_out) -> ReplayParams:
+    """Fill ``ssd_replay_params`` (the scan part from ``make_params`` with
+    ``write_final=False``)."""
+    torch = _torch()
+    r = ReplayParams()
+    r.scan = scan
+    r.ring_x, r.ring_B = _ptr(ring_x), _ptr(ring_B)
+    r.ring_dt = _ptr(ring_dt, torch.float32)
+    r.ring_capacity = ring_x.shape[1]
+    r.ring_window = int(ring_window)
+    r.ring_start, r.ring_count = _ptr(ring_start, torch.int32), _ptr(ring_count, torch.int32)
+    r.ring_start_out = _ptr(ring_start_out, torch.int32)
+    r.ring_count_out = _ptr(ring_count_out, torch.int32)
+    return r
+
+
+def call_replay(params: ReplayParams, stream_ptr: int = 0) -> None:
+    rc = load().ssd_replay_mtp(ctypes.byref(params), ctypes.c_void_p(stream_ptr or None))
+    if rc != SSD_OK:
+        raise SSDError(rc)
+
+
+def set_test_hooks(wait_cycles: int = 0, withhold_handover: int = -1,
+                   force_unsegmented: bool = False) -> None:
+    """``ssd_testing_set_hooks`` (tests of the failure detection only)."""
+    load().ssd_testing_set_hooks(int(wait_cycles), int(withhold_handover), int(bool(force_unsegmented)))
 
 
 def call_noalloc(params: ScanParams, stream_ptr: int = 0) -> None:

@@ -61,10 +61,13 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstddef>
 #include <mutex>
+#include <type_traits>
 
 #include "sm100.cuh"
+#include "ssd_common.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
@@ -121,6 +124,18 @@ struct Params {
     void *state_cache, *out_y;
     const void *x;
     int32_t *device_status;
+    // optional parts of a call
+    const int32_t *final_slot_idx;                // NULL: final states to slot_idx
+    int64_t slot_stride, final_slot_stride;       // elements between entries (>= 1)
+    const int32_t *snap_flag;                     // snapshot pass: initial state copied
+    const void *snap_states;                      //   to snap_states[s] (cache dtype)
+    void *out_chunk_states;                       // per-chunk states (NULL: off)
+    const int32_t *cu_chunks;
+    int32_t num_chunk_rows, chunk_size;           // chunk_size a multiple of kQ here
+    const uint64_t *sr_seed;                      // fp16 cache: stochastic rounding
+    // failure-detection test hooks (see ssd_testing_set_hooks)
+    uint64_t spin_limit;                          // clock cycles per wait
+    int32_t withhold;                             // hand-over never published, -1: none
 };
 
 // per-block decay arrays, written by the dt warp two blocks ahead
@@ -151,7 +166,11 @@ struct __align__(16) Item {
     int32_t round;                // deal round after this item
     int32_t seq, h0, g, slot, t0, len, bin, bout;
     int32_t flags;                // bit 0: found, 1: initial state, 2: from the workspace,
-                                  // 3: final state to the workspace
+                                  // 3: final state to the workspace, 4: initial state
+                                  // from the snapshot
+    int32_t fslot;                // slot the final state goes to
+    int32_t seq_t0;               // first token of the sequence (chunk boundaries)
+    int32_t crow;                 // first per-chunk state row of the sequence, -1: none
 };
 constexpr int kItemRing = 8;      // items looked up ahead by the item warp
 constexpr int kSortInCta = 32;    // batches of up to this many sequences are sorted in the kernel
@@ -174,6 +193,7 @@ struct __align__(1024) Smem {
     int32_t order_small[kSortInCta];      // longest-first order when the item warp sorts
     uint32_t tmem_base;
     int32_t abort_flag;
+    uint64_t spin_limit;          // clock cycles a wait may take before it gives up
 };
 
 // Vector (8/16-byte) shared-memory accesses rely on these offsets.
@@ -189,13 +209,14 @@ static_assert(offsetof(Smem, xw) % 1024 == 0 && offsetof(Smem, hbuf) % 1024 == 0
 // work enumeration, identical in every role
 // ---------------------------------------------------------------------------
 struct Chunk {
-    int32_t seq, h0, g, slot;
+    int32_t seq, h0, g, slot, fslot, seq_t0, crow;
     int32_t row0;        // first token of this block (total tokens < 2^31 on this path)
     int32_t l;           // valid tokens in this block
     int32_t bin, bout;   // workspace state slots read at the first / written at the last block
     bool init, first, last, empty_item;
     bool init_ws;        // the initial state comes from the workspace (a previous segment)
     bool fin_ws;         // the final state goes to the workspace (a following segment)
+    bool snap;           // the initial state comes from the snapshot of the cache slot
 };
 
 // Next valid item of this CTA (longest sequences first, snake order over the
@@ -234,15 +255,26 @@ __device__ __noinline__ Item find_item(const Params &p, const int32_t *order, in
             continue;
         }
         const bool init = p.has_init != nullptr && p.has_init[seq] != 0;
-        int32_t slot = 0;
+        int32_t slot = 0, fslot = 0;
         if (init || p.write_final) {
-            slot = p.slot_idx[seq];
-            if (slot < 0 || slot >= p.num_slots) {
+            slot = p.slot_idx[seq * p.slot_stride];
+            fslot = (p.write_final && p.final_slot_idx) ? p.final_slot_idx[seq * p.final_slot_stride] : slot;
+            if ((init && (slot < 0 || slot >= p.num_slots)) ||
+                (p.write_final && (fslot < 0 || fslot >= p.num_slots))) {
                 if (report && j == 0 && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SLOT);
                 continue;
             }
         }
         const int32_t len = (int32_t)(e - a);
+        int32_t crow = -1;
+        if (p.out_chunk_states) {
+            const int64_t c0 = p.cu_chunks[seq], c1 = p.cu_chunks[seq + 1];
+            if (c0 >= 0 && c1 - c0 == (len + p.chunk_size - 1) / p.chunk_size && c1 <= p.num_chunk_rows)
+                crow = (int32_t)c0;
+            else if (report && j == 0 && p.device_status)
+                atomicOr(p.device_status, SSD_DEV_BAD_CHUNKS);
+        }
+        const bool snap = init && p.snap_flag != nullptr && p.snap_flag[seq] != 0;
         const int32_t nb = (len + kQ - 1) / kQ;
         const int32_t nseg = nb == 0 ? 1 : (nb + seg - 1) / seg;
         const int32_t b0 = j * seg, b1 = min(nb, (j + 1) * seg);
@@ -254,7 +286,11 @@ __device__ __noinline__ Item find_item(const Params &p, const int32_t *order, in
         it.len = nb == 0 ? 0 : min(len, b1 * kQ) - b0 * kQ;
         it.bin = j > 0 ? (p.bstart[rank] + j - 1) * hp_per_seq + hp : 0;
         it.bout = j + 1 < nseg ? (p.bstart[rank] + j) * hp_per_seq + hp : 0;
-        it.flags = 1 | ((j > 0 || init) ? 2 : 0) | (j > 0 ? 4 : 0) | (j + 1 < nseg ? 8 : 0);
+        it.flags = 1 | ((j > 0 || init) ? 2 : 0) | (j > 0 ? 4 : 0) | (j + 1 < nseg ? 8 : 0) |
+                   ((j == 0 && snap) ? 16 : 0);
+        it.fslot = fslot;
+        it.seq_t0 = (int32_t)a;
+        it.crow = crow;
         break;
     }
     it.round = round;
@@ -274,7 +310,7 @@ __device__ __noinline__ bool wait_bar_slow(Smem &sm, uint64_t *bar, uint32_t par
     while (!mbar_try_wait(bar, parity)) {
         if ((++it & 255u) == 0) {
             if (*(volatile int32_t *)&sm.abort_flag) return false;
-            if (clock64() - t_start > kSpinLimit) {
+            if (clock64() - t_start > sm.spin_limit) {
                 atomicExch(&sm.abort_flag, 1);
                 if (status) atomicOr(status, SSD_DEV_TIMEOUT);
                 return false;
@@ -282,6 +318,19 @@ __device__ __noinline__ bool wait_bar_slow(Smem &sm, uint64_t *bar, uint32_t par
         }
     }
     return true;
+}
+
+// Wait for this CTA's own asynchronous work (TMA loads, MMAs) before it exits.
+// Bounded like every wait, but not cut short by the abort flag: that work ends
+// by itself and must not outlive the CTA's shared and tensor memory.
+__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+    const uint64_t t_start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t_start > kSpinLimit) {
+            if (status) atomicOr(status, SSD_DEV_TIMEOUT);
+            return;
+        }
+    }
 }
 
 // Single-thread wait (producer / MMA issuer).
@@ -299,7 +348,7 @@ __device__ __noinline__ bool warp_wait_slow(Smem &sm, uint64_t *bar, uint32_t pa
             if ((threadIdx.x & 31) == 0) {
                 if (*(volatile int32_t *)&sm.abort_flag) {
                     give_up = 1;
-                } else if (clock64() - t_start > kSpinLimit) {
+                } else if (clock64() - t_start > sm.spin_limit) {
                     atomicExch(&sm.abort_flag, 1);
                     if (status) atomicOr(status, SSD_DEV_TIMEOUT);
                     give_up = 1;
@@ -337,7 +386,7 @@ __device__ __noinline__ bool warp_wait_flag(Smem &sm, const int32_t *flag, int32
             if ((threadIdx.x & 31) == 0) {
                 if (*(volatile int32_t *)&sm.abort_flag) {
                     give_up = 1;
-                } else if (clock64() - t_start > kSpinLimit) {
+                } else if (clock64() - t_start > sm.spin_limit) {
                     atomicExch(&sm.abort_flag, 1);
                     if (status) atomicOr(status, SSD_DEV_TIMEOUT);
                     give_up = 1;
@@ -401,9 +450,11 @@ struct Walker {
 
     __device__ void fill(Chunk &c) const {
         c.seq = it.seq; c.h0 = it.h0; c.g = it.g; c.slot = it.slot;
+        c.fslot = it.fslot; c.seq_t0 = it.seq_t0; c.crow = it.crow;
         c.init = (it.flags & 2) != 0;
         c.init_ws = (it.flags & 4) != 0;
         c.fin_ws = (it.flags & 8) != 0;
+        c.snap = (it.flags & 16) != 0;
         c.bin = it.bin;
         c.bout = it.bout;
     }
@@ -481,6 +532,23 @@ template <> __device__ __forceinline__ void store_state<__nv_bfloat16>(__nv_bflo
 template <> __device__ __forceinline__ void store_state<__half>(__half *p, float v) {
     *p = __float2half_rn(v);
 }
+// One state value at flat element index e of a [rows, H, P, N] tensor: nearest
+// even, or for fp16 with a seed stochastic rounding with the element's Philox
+// word (stream 0: the cache, 1: per-chunk states).
+// Out of line: the generator's ten rounds stay out of the state warps' hot code.
+__device__ __noinline__ void put_state_sr(__half *base, int64_t e, float v, uint64_t seed, uint32_t stream) {
+    base[e] = sr_f16(v, sr_word(sr_block(seed, (uint64_t)e >> 2, stream), (uint32_t)(e & 3)));
+}
+template <typename StT>
+__device__ __forceinline__ void put_state(StT *base, int64_t e, float v, bool sr, uint64_t seed, uint32_t stream) {
+    if constexpr (std::is_same<StT, __half>::value) {
+        if (sr) {
+            put_state_sr(base, e, v, seed, stream);
+            return;
+        }
+    }
+    store_state<StT>(base + e, v);
+}
 
 // ---------------------------------------------------------------------------
 // launch 1: longest-first order of the sequences
@@ -498,11 +566,10 @@ constexpr int kPrepSmem = kSortMax * (int)sizeof(unsigned long long);   // dynam
 // (boundaries x head pairs, the workspace's capacity).  Writes order[S], and
 // with segmentation meta
 // (item count, seg, levels, level offsets), bstart[rank] (first boundary of
-// each sequence) and clears the boundary flags of this call.
-__global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t *cu, int S, int64_t T,
-                                                                    int32_t *order, int32_t *meta,
-                                                                    int32_t *bstart, int32_t *flags, int hp,
-                                                                    int num_sms, int cap, int seg_enabled) {
+// each sequence) and clears the boundary flags of this call.  Run by CTA 0.
+__device__ __noinline__ void prep_order(const int32_t *cu, int S, int64_t T, int32_t *order, int32_t *meta,
+                                        int32_t *bstart, int32_t *flags, int hp, int num_sms, int cap,
+                                        int seg_enabled) {
     // sort keys: (2^31 - 1 - block count) << 32 | sequence, ascending = longest
     // first, ties by sequence index
     extern __shared__ unsigned long long keys[];
@@ -622,6 +689,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t 
         meta[0] = offs;
         meta[1] = seg;
         meta[2] = nlev;
+    }
+}
+
+// Launch 1: the order (CTA 0, when the scan kernel does not sort the batch
+// itself) and, for calls whose sequences may read a slot another sequence
+// writes, the snapshot of those initial states (every CTA, a sequence each).
+__global__ void __launch_bounds__(kPrepThreads) prep_order_kernel(const int32_t *cu, int S, int64_t T,
+                                                                    int32_t *order, int32_t *meta,
+                                                                    int32_t *bstart, int32_t *flags, int hp,
+                                                                    int num_sms, int cap, int seg_enabled,
+                                                                    int do_sort, SnapshotArgs snap,
+                                                                    int do_snap) {
+    if (do_sort && blockIdx.x == 0) prep_order(cu, S, T, order, meta, bstart, flags, hp, num_sms, cap, seg_enabled);
+    if (do_snap) {
+        __shared__ int conflict;
+        for (int s = blockIdx.x; s < snap.S; s += gridDim.x) snapshot_sequence(snap, s, &conflict);
     }
 }
 
@@ -807,6 +890,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             mbar_init(&sm.item_empty[i], kItemTakers);
         }
         sm.abort_flag = 0;
+        sm.spin_limit = p.spin_limit;
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -858,7 +942,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 ++kc;
             }
             for (uint32_t t = (issued > (uint32_t)kSlots ? issued - kSlots : 0); t < issued; ++t)
-                wait_bar(sm, &sm.full[t % kSlots], (t / kSlots) & 1, nullptr);
+                drain_wait(&sm.full[t % kSlots], (t / kSlots) & 1, status);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer, output path =====================
@@ -945,7 +1029,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 ++kc;
             }
             mma_commit(&sm.drain_y);
-            wait_bar(sm, &sm.drain_y, 0, nullptr);
+            drain_wait(&sm.drain_y, 0, status);
         }
     } else if (warp == 3) {
         // ===================== item dealer =====================
@@ -985,7 +1069,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             if (x.init_ws)
                 bulk_prefetch_l2(p.seg_state + (size_t)x.bin * (2 * kP * kN), 2 * kP * kN * sizeof(float));
             else
-                bulk_prefetch_l2(static_cast<const StT *>(p.state_cache) + ((int64_t)x.slot * p.H + x.h0) * (kP * kN),
+                bulk_prefetch_l2(static_cast<const StT *>(x.snap ? p.snap_states : p.state_cache) +
+                                     ((int64_t)(x.snap ? x.seq : x.slot) * p.H + x.h0) * (kP * kN),
                                  2 * kP * kN * sizeof(StT));
         };
         bool have = wk.next(sm, c, false, true, status);
@@ -1101,7 +1186,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         }
         if (warp == 4 && lane == 0) {                          // the state MMAs' issuing thread
             mma_commit(&sm.drain_h);
-            wait_bar(sm, &sm.drain_h, 0, nullptr);
+            drain_wait(&sm.drain_h, 0, status);
         }
     } else if (warp >= 8 && warp < 12) {
         // ===================== S and row scaling (lane = token) =====================
@@ -1230,11 +1315,14 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         auto publish = [&]() {
             __threadfence();
             __syncwarp();
-            if (lane == 0) st_release_gpu(p.seg_flags + (size_t)(pend - 1) * 4 + q, 1);
+            if (lane == 0 && pend - 1 != p.withhold) st_release_gpu(p.seg_flags + (size_t)(pend - 1) * 4 + q, 1);
             pend = 0;
         };
         bool ok = true;
         StT *cache = static_cast<StT *>(p.state_cache);
+        StT *chunk_out = static_cast<StT *>(p.out_chunk_states);
+        const bool sr = std::is_same<StT, __half>::value && p.sr_seed != nullptr;
+        const uint64_t seed = sr ? *p.sr_seed : 0ull;
         int32_t prev_row0 = 0, prev_l = 0, prev_h0 = 0;   // previous block, for its y epilogue
         // y = Y + D x of block k (lane = token t here; x from the smem tile, which
         // stays until x_epi_done), run while block k+1's state MMAs execute
@@ -1283,12 +1371,20 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             return true;
         };
         while (ok && wk.next(sm, c, true, true, status)) {
-            const int64_t hbase = ((int64_t)c.slot * p.H + c.h0) * (kP * kN) + n;   // + (head*64+p)*N
+            // this lane's column (+ (head*64+p)*N) of the initial state (the cache
+            // slot, or its snapshot) and the element index of the final slot's
+            auto init_col = [&]() {
+                return (c.snap ? static_cast<const StT *>(p.snap_states) : cache) +
+                       ((int64_t)(c.snap ? c.seq : c.slot) * p.H + c.h0) * (kP * kN) + n;
+            };
+            auto final_base = [&]() { return ((int64_t)c.fslot * p.H + c.h0) * (kP * kN) + n; };
             if (c.empty_item) {
+                const StT *init_src = init_col();
+                const int64_t fbase = final_base();
                 if (p.write_final) {
                     for (int col = 0; col < 2 * kP; ++col) {
-                        const float v = c.init ? load_state<StT>(cache + hbase + (int64_t)col * kN) : 0.f;
-                        store_state<StT>(cache + hbase + (int64_t)col * kN, v);
+                        const float v = c.init ? load_state<StT>(init_src + (int64_t)col * kN) : 0.f;
+                        put_state<StT>(cache, fbase + (int64_t)col * kN, v, sr, seed, 0u);
                     }
                 }
                 continue;
@@ -1330,9 +1426,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
 #pragma unroll
                         for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__ldcg(ws + (j * 64 + i) * kN));
                     } else {
+                        const StT *init_src = init_col();
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            r[i] = __float_as_uint(load_state<StT>(cache + hbase + (int64_t)(j * 64 + i) * kN));
+                            r[i] = __float_as_uint(load_state<StT>(init_src + (int64_t)(j * 64 + i) * kN));
                     }
                     tmem_st32(tmem + lane_off + kColH + 64 * j, *reinterpret_cast<const uint32_t(*)[32]>(r));
                     tmem_st32(tmem + lane_off + kColH + 64 * j + 32, *reinterpret_cast<const uint32_t(*)[32]>(r + 32));
@@ -1349,6 +1446,24 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             const bool rn0 = ar.renorm[0] != 0, rn1 = ar.renorm[1] != 0;
             if (kc > 0 && !(ok = warp_wait(sm, &sm.hlo_free, (kc - 1) & 1, status))) break;
             uint8_t *lorow = sm.hlo[n >> 6] + hrow * 128;
+            // the state entering this block ends a chunk of the sequence: store it
+            // (its own pass over the accumulator, before the copies below take
+            // their registers)
+            const int32_t pos0 = c.row0 - c.seq_t0;
+            if (chunk_out != nullptr && c.crow >= 0 && !c.first && pos0 % p.chunk_size == 0) {
+                const int64_t cbase = ((int64_t)(c.crow + pos0 / p.chunk_size - 1) * p.H + c.h0) * (kP * kN) + n;
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lane_off + kColH + 16 * j, r);
+                    tmem_wait_ld();
+                    const float e = (j >> 2) ? ar.eprev[1] : ar.eprev[0];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        put_state<StT>(chunk_out, cbase + (int64_t)(j * 16 + i) * kN, __uint_as_float(r[i]) * e, sr,
+                                       seed, 1u);
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {                 // 16 columns at a time
                 uint32_t r[16];
@@ -1444,7 +1559,17 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                         }
                     }
                     pend = c.bout + 1;            // published once the next block's h copy is out
-                } else if (p.write_final) {
+                }
+                // the item's end: the sequence's end, or a segment cut that may
+                // also end a chunk
+                const int32_t pos1 = c.row0 + c.l - c.seq_t0;
+                const bool cend = chunk_out != nullptr && c.crow >= 0 &&
+                                  (!c.fin_ws || pos1 % p.chunk_size == 0);
+                const int64_t cbase_end =
+                    ((int64_t)(c.crow + (pos1 - 1) / p.chunk_size) * p.H + c.h0) * (kP * kN) + n;
+                const bool fin = !c.fin_ws && p.write_final;
+                const int64_t fbase = final_base();
+                if (fin || cend) {
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
                         uint32_t r[32];
@@ -1454,8 +1579,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
 #pragma unroll
                         for (int i2 = 0; i2 < 16; ++i2) {
                             const float2 h = __fmul2_rn(f2(r[2 * i2], r[2 * i2 + 1]), ef);
-                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + 2 * i2) * kN, h.x);
-                            store_state<StT>(cache + hbase + (int64_t)(j * 32 + 2 * i2 + 1) * kN, h.y);
+                            const int64_t col = j * 32 + 2 * i2;
+                            if (fin) {
+                                put_state<StT>(cache, fbase + col * kN, h.x, sr, seed, 0u);
+                                put_state<StT>(cache, fbase + (col + 1) * kN, h.y, sr, seed, 0u);
+                            }
+                            if (cend) {
+                                put_state<StT>(chunk_out, cbase_end + col * kN, h.x, sr, seed, 1u);
+                                put_state<StT>(chunk_out, cbase_end + (col + 1) * kN, h.y, sr, seed, 1u);
+                            }
                         }
                     }
                 }
@@ -1517,6 +1649,11 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
+
+// failure-detection test hooks (ssd_testing_set_hooks)
+std::atomic<uint64_t> g_hook_wait_cycles{0};
+std::atomic<int32_t> g_hook_withhold{-1};
+std::atomic<int32_t> g_hook_force_unsegmented{0};
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
@@ -1629,11 +1766,18 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
     int32_t *bstart = seg ? reinterpret_cast<int32_t *>(ws + L.bstart) : nullptr;
     int32_t *flags = seg ? reinterpret_cast<int32_t *>(ws + L.flags) : nullptr;
     float *states = seg ? reinterpret_cast<float *>(ws + L.states) : nullptr;
-    // Small unsegmented batches are sorted by the scan kernel itself: one launch.
+    // Small unsegmented batches are sorted by the scan kernel itself: one launch
+    // unless the initial states need a snapshot.
     const bool sort_in_cta = !seg && a.S <= kSortInCta;
-    if (!sort_in_cta) {
-        prep_order_kernel<<<1, kPrepThreads, kPrepSmem, stream>>>(a.cu_seqlens, a.S, a.T, order, meta, bstart,
-                                                                   flags, hp, sms, L.cap, seg ? 1 : 0);
+    const bool snap = a.snap_flag != nullptr;
+    if (!sort_in_cta || snap) {
+        const SnapshotArgs sa = make_snapshot_args(a, st_idx == 0 ? SSD_F32 : st_idx == 1 ? SSD_BF16 : SSD_F16,
+                                                   const_cast<int32_t *>(a.snap_flag),
+                                                   const_cast<void *>(a.snap_states));
+        const int pgrid = snap ? std::min(a.S, 4096) : 1;
+        prep_order_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(a.cu_seqlens, a.S, a.T, order, meta, bstart,
+                                                                       flags, hp, sms, L.cap, seg ? 1 : 0,
+                                                                       sort_in_cta ? 0 : 1, sa, snap ? 1 : 0);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1666,7 +1810,26 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
     p.out_y = a.out_y;
     p.x = a.x;
     p.device_status = a.device_status;
+    p.final_slot_idx = a.final_slot_idx;
+    p.slot_stride = a.slot_stride ? a.slot_stride : 1;
+    p.final_slot_stride = a.final_slot_stride ? a.final_slot_stride : 1;
+    p.snap_flag = a.snap_flag;
+    p.snap_states = a.snap_states;
+    p.out_chunk_states = a.out_chunk_states;
+    p.cu_chunks = a.cu_chunks;
+    p.num_chunk_rows = a.num_chunk_rows;
+    p.chunk_size = a.chunk_size;
+    p.sr_seed = a.sr_seed;
+    const uint64_t hook_wait = g_hook_wait_cycles.load();
+    p.spin_limit = hook_wait ? hook_wait : kSpinLimit;
+    p.withhold = g_hook_withhold.load();
     const int grid = p.num_items < sms ? p.num_items : sms;
+    if (seg && g_hook_force_unsegmented.load()) {
+        // test hook: the path taken when the cooperative launch is refused
+        p.seg_enabled = 0;
+        chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
+        return cudaGetLastError();
+    }
     if (!seg) {
         chunked_scan_kernel<StT><<<grid, kThreads, kSmemBytes, stream>>>(mx, mb, mc, p);
         return cudaGetLastError();
@@ -1695,8 +1858,16 @@ cudaError_t launch_typed(const ScanArgs &a, int st_idx, void *workspace, size_t 
 
 }  // namespace
 
+void set_test_hooks(int64_t wait_cycles, int32_t withhold, int32_t force_unsegmented) {
+    g_hook_wait_cycles.store(wait_cycles > 0 ? (uint64_t)wait_cycles : 0);
+    g_hook_withhold.store(withhold);
+    g_hook_force_unsegmented.store(force_unsegmented ? 1 : 0);
+}
+
 bool chunked_supported(const ssd_scan_params &p) {
     if (p.io_dtype != SSD_BF16 || p.headdim != kP || p.dstate != kN) return false;
+    // per-chunk states fall on 128-token block ends only
+    if (p.out_chunk_states != nullptr && p.chunk_size % kQ != 0) return false;
     if (p.nheads % 2 != 0 || (p.nheads / p.ngroups) % 2 != 0) return false;
     if (p.total_tokens >= (1LL << 31) - kQ) return false;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.B) |
@@ -1715,7 +1886,7 @@ int32_t chunked_num_launches(const ssd_scan_params &p, size_t workspace_bytes) {
     int sms = 0;
     if (current_device_sms(&sms) != cudaSuccess) return -1;
     const bool seg = may_segment(p.total_tokens, p.num_seqs, p.nheads, p.max_seqlen, workspace_bytes, sms);
-    return (!seg && p.num_seqs <= kSortInCta) ? 1 : 2;
+    return (!seg && p.num_seqs <= kSortInCta && !snapshot_needed(p)) ? 1 : 2;
 }
 
 cudaError_t launch_chunked(const ScanArgs &a, int state_dtype, void *workspace, size_t workspace_bytes,

@@ -14,41 +14,34 @@
 // Costs and limits:
 //  * every GPU that loads the library holds the array (kNoallocMaxSeqs
 //    int32 = 256 KiB) until the process exits;
-//  * batches of more than kNoallocMaxSeqs sequences are rejected with
-//    SSD_ERR_SCRATCH_LIMIT before anything is enqueued;
-//  * the first call on a device looks up the array's device address (with
-//    that device current) -- make that first call before any stream capture;
+//  * on the tensor-core path, batches of more than kNoallocMaxSeqs sequences
+//    are rejected with SSD_ERR_SCRATCH_LIMIT before anything is enqueued (the
+//    token-by-token path needs no scratch and takes any batch);
+//  * the array has no room for the snapshot of initial states that calls
+//    with crossed or shared slots need: such calls are rejected with
+//    SSD_ERR_SCRATCH_LIMIT unless the caller sets slots_disjoint;
+//  * every call looks the array's device address up with the call's device
+//    current (a host-side lookup; the first one on a device may load the
+//    library's module, so make it before any stream capture).  Not caching the
+//    address keeps a call correct after the device was reset and the module
+//    reloaded elsewhere;
 //  * all calls share the one array: two calls whose kernels overlap on the
 //    GPU (different streams, no ordering between them) race on it.  The
 //    kernels rewrite every entry they read, so nothing has to start at zero.
-#include <mutex>
-
 #include "ssd_internal.h"
 
 namespace {
 
 constexpr int kNoallocMaxSeqs = SSD_NOALLOC_MAX_SEQS;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocMaxSeqs];
 
-std::mutex g_setup_mu;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device.
 cudaError_t scratch_for_current_device(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = ptr;
-    }
-    *out = g_scratch_addr[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 
@@ -59,15 +52,13 @@ extern "C" ssd_status ssd_scan_varlen_noalloc(const ssd_scan_params *params,
     const ssd_status v = ssd::detail::validate(params);
     if (v != SSD_OK) return v;
     if (params->num_seqs == 0) return SSD_OK;
-    if (params->num_seqs > kNoallocMaxSeqs) return SSD_ERR_SCRATCH_LIMIT;
-    const ssd::ScanArgs a = ssd::detail::make_args(params);
-    cudaError_t err;
-    if (ssd::detail::use_chunked(params)) {
-        void *scratch = nullptr;
-        err = scratch_for_current_device(&scratch);
-        if (err == cudaSuccess) err = ssd::launch_chunked(a, params->state_dtype, scratch, sizeof(g_noalloc_scratch), stream);
-    } else {
-        err = ssd::launch_recurrent(a, params->io_dtype, params->state_dtype, stream);
+    if (ssd::snapshot_needed(*params)) return SSD_ERR_SCRATCH_LIMIT;
+    const bool chunked = ssd::detail::use_chunked(params);
+    if (chunked && params->num_seqs > kNoallocMaxSeqs) return SSD_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (chunked) {
+        const cudaError_t err = scratch_for_current_device(&scratch);
+        if (err != cudaSuccess) return SSD_ERR_CUDA;
     }
-    return err == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    return ssd::detail::run(params, scratch, chunked ? sizeof(g_noalloc_scratch) : 0, stream);
 }

@@ -12,12 +12,23 @@
 // columns n, so the whole state slice lives in registers (4 x NPL floats per
 // thread) and one token costs one warp-level reduction per p-row for y.
 // Warps never synchronise with each other.  The initial state is read
-// straight from the cache slot (no gather, vLLM PR #62922 "Details") and the
-// final state is written back into the same slot in the cache dtype with
-// round-to-nearest-even (vLLM PR #61501 "Details").
+// straight from the cache slot (no gather, vLLM PR #62922 "Details"), or from
+// the snapshot the snapshot pass took when another sequence of the call writes
+// that slot, and the final state is written back in the cache dtype with
+// round-to-nearest-even (vLLM PR #61501 "Details") or stochastic rounding.
+// Optionally the state after every token (MTP) or at every chunk boundary
+// (checkpoint prefill) is written as well.
+//
+// The same kernel runs the ReplaySSM verification step (vLLM PR #52928
+// "Summary"): before the window tokens it advances the checkpoint through the
+// pending ring inputs, folds them into the checkpoint when the window would
+// overflow the ring, and appends the window's inputs to the ring.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
+#include "ssd_common.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
@@ -99,7 +110,11 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 // kDepth: tokens of input prefetched ahead of the recurrence (a register ring;
 // deeper for narrow states, where registers are cheap and the chain is short).
-template <typename IoT, typename StT, int NPL, int kDepth>
+// kFull: the optional parts of a call (separate final slots, strided slot
+// indices, snapshot reads, per-chunk states, stochastic rounding, the
+// ReplaySSM ring) are compiled in; calls without them run the plain variant,
+// whose register budget they would otherwise take.
+template <typename IoT, typename StT, int NPL, int kDepth, bool kFull>
 __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -113,23 +128,57 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const int g = h / a.heads_per_group;
 
     // ---- sequence metadata, checked on the device (loads issued together) ----
+    const bool replay = kFull && a.ring_x != nullptr;
+    const bool reporter = threadIdx.x == 0 && pb == 0 && h == 0;
     const int64_t t0 = a.cu_seqlens[s];
     const int64_t t1 = a.cu_seqlens[s + 1];
-    const bool init = a.has_init != nullptr && a.has_init[s] != 0;
-    const int slot_raw = a.slot_idx != nullptr ? a.slot_idx[s] : 0;
+    const bool init = replay || (a.has_init != nullptr && a.has_init[s] != 0);
+    const int64_t sstride = kFull && a.slot_stride ? a.slot_stride : 1;
+    const int slot_raw = a.slot_idx != nullptr ? a.slot_idx[s * sstride] : 0;
+    const int fslot_raw = (kFull && a.write_final && a.final_slot_idx != nullptr)
+                              ? a.final_slot_idx[s * (a.final_slot_stride ? a.final_slot_stride : 1)]
+                              : slot_raw;
     if (t0 < 0 || t1 < t0 || t1 > a.T) {
-        if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
-            atomicOr(a.device_status, SSD_DEV_BAD_SEQLENS);
+        if (reporter && a.device_status) atomicOr(a.device_status, SSD_DEV_BAD_SEQLENS);
         return;
     }
-    const bool need_slot = init || a.write_final;
-    int slot = 0;
-    if (need_slot) {
-        slot = slot_raw;
-        if (slot < 0 || slot >= a.num_slots) {
-            if (threadIdx.x == 0 && pb == 0 && h == 0 && a.device_status)
-                atomicOr(a.device_status, SSD_DEV_BAD_SLOT);
+    int slot = 0, fslot = 0;
+    if ((init && (slot_raw < 0 || slot_raw >= a.num_slots)) ||
+        (a.write_final && (fslot_raw < 0 || fslot_raw >= a.num_slots))) {
+        if (reporter && a.device_status) atomicOr(a.device_status, SSD_DEV_BAD_SLOT);
+        return;
+    }
+    if (init) slot = slot_raw;
+    if (a.write_final) fslot = fslot_raw;
+    // per-chunk states: rows cu_chunks[s] .. cu_chunks[s+1]-1
+    StT *chunks = kFull ? static_cast<StT *>(a.out_chunk_states) : nullptr;
+    int64_t crow0 = 0;
+    if (chunks) {
+        const int64_t c0 = a.cu_chunks[s], c1 = a.cu_chunks[s + 1];
+        const int64_t nch = (t1 - t0 + a.chunk_size - 1) / a.chunk_size;
+        if (c0 < 0 || c1 - c0 != nch || c1 > a.num_chunk_rows) {
+            if (reporter && a.device_status) atomicOr(a.device_status, SSD_DEV_BAD_CHUNKS);
+            chunks = nullptr;
+        }
+        crow0 = c0;
+    }
+    // ReplaySSM: pending ring inputs and where the window goes
+    int32_t rcount = 0, rstart = 0, wpos0 = 0;
+    bool fold = false;
+    if (replay) {
+        rcount = a.ring_count[s];
+        rstart = a.ring_start[s];
+        const int64_t K = t1 - t0;
+        if (rcount < 0 || rcount > a.ring_window || rstart < 0 || rstart >= a.ring_capacity ||
+            K > (int64_t)a.ring_capacity - a.ring_window) {
+            if (reporter && a.device_status) atomicOr(a.device_status, SSD_DEV_BAD_RING);
             return;
+        }
+        fold = rcount + K > a.ring_window;
+        wpos0 = (rstart + rcount) % a.ring_capacity;
+        if (reporter) {
+            a.ring_start_out[s] = fold ? wpos0 : rstart;
+            a.ring_count_out[s] = fold ? 0 : rcount;
         }
     }
 
@@ -140,13 +189,17 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
 
     // ---- initial state (fp32 in registers) ---------------------------------
     float st[kRowsPerWarp][NPL];
-    const StT *cache = static_cast<const StT *>(a.state_cache);
-    const int64_t slot_base = (((int64_t)slot * a.H + h) * a.P) * a.N;
+    const int64_t head_off = ((int64_t)h * a.P) * a.N;
+    const int64_t slot_base = (int64_t)slot * a.H * a.P * a.N + head_off;
+    const int64_t fslot_base = (int64_t)fslot * a.H * a.P * a.N + head_off;
+    const StT *src = static_cast<const StT *>(a.state_cache) + slot_base;
+    if (kFull && a.snap_flag != nullptr && a.snap_flag[s] != 0)
+        src = static_cast<const StT *>(a.snap_states) + (int64_t)s * a.H * a.P * a.N + head_off;
     const int nvalid = a.N - n0;           // columns of this lane inside [0, N)
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
         if (init && row_ok[i]) {
-            load_n<StT, NPL>(cache + slot_base + (int64_t)(p0 + i) * a.N + n0, st[i], nvalid, vec);
+            load_n<StT, NPL>(src + (int64_t)(p0 + i) * a.N + n0, st[i], nvalid, vec);
         } else {
 #pragma unroll
             for (int j = 0; j < NPL; ++j) st[i][j] = 0.f;
@@ -161,6 +214,65 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const float Ah = a.A[h];
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const float Dh = a.D ? a.D[h] : 0.f;
+    const int nw = nvalid < NPL ? (nvalid > 0 ? nvalid : 0) : NPL;
+    // this warp's rows of the state (cache dtype; stochastic rounding for fp16
+    // with a seed), at flat element index base of a [rows, H, P, N] tensor
+    auto store_rows = [&](StT *dst, int64_t base, uint32_t stream) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            if (!row_ok[i] || nw == 0) continue;
+            const int64_t e = base + (int64_t)(p0 + i) * a.N + n0;
+            if constexpr (kFull && std::is_same<StT, __half>::value) {
+                if (a.sr_seed != nullptr) {
+                    StateStore<StT>::run(dst + e, st[i], nw, (uint64_t)e, a.sr_seed, stream);
+                    continue;
+                }
+            }
+            store_n<StT, NPL>(dst + e, st[i], nvalid, vec);
+        }
+    };
+    // the state after token t, when t ends a chunk of its sequence
+    auto chunk_store = [&](int64_t t) {
+        const int64_t pos = t - t0;
+        if (chunks && ((pos + 1) % a.chunk_size == 0 || t == t1 - 1))
+            store_rows(chunks, ((crow0 + pos / a.chunk_size) * a.H) * a.P * a.N + head_off, 1u);
+    };
+    // ReplaySSM: the window token t goes to ring position wpos0 + (t - t0)
+    auto ring_store = [&](int64_t t) {
+        if (!replay) return;
+        const int64_t pos = (wpos0 + (t - t0)) % a.ring_capacity;
+        const int64_t rrow = (int64_t)slot * a.ring_capacity + pos;
+        if (lane < kRowsPerWarp && row_ok[lane])
+            static_cast<IoT *>(a.ring_x)[(rrow * a.H + h) * a.P + p0 + lane] = X[(t * a.H + h) * a.P + p0 + lane];
+        if (pb == 0 && warp == 0) {
+            if (lane == 0) a.ring_dt[rrow * a.H + h] = a.dt[t * a.H + h];
+            if (h % a.heads_per_group == 0)
+                for (int j = 0; j < NPL; ++j)
+                    if (n0 + j < a.N)
+                        static_cast<IoT *>(a.ring_B)[(rrow * a.G + g) * a.N + n0 + j] =
+                            Bm[(t * a.G + g) * a.N + n0 + j];
+        }
+    };
+    if (replay) {
+        // advance the checkpoint through the pending ring inputs (no output)
+        for (int32_t j = 0; j < rcount; ++j) {
+            const int64_t rrow = (int64_t)slot * a.ring_capacity + (rstart + j) % a.ring_capacity;
+            const float z = a.ring_dt[rrow * a.H + h] + bias;
+            const float d = a.dt_softplus ? softplus_f(z) : z;
+            const float decay = expf(d * Ah);
+            float xv[kRowsPerWarp], bv[NPL];
+            load_n<IoT, kRowsPerWarp>(static_cast<const IoT *>(a.ring_x) + (rrow * a.H + h) * a.P + p0, xv,
+                                      a.P - p0, vec);
+            load_n<IoT, NPL>(static_cast<const IoT *>(a.ring_B) + (rrow * a.G + g) * a.N + n0, bv, nvalid, vec);
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const float dx = d * xv[i];
+#pragma unroll
+                for (int j = 0; j < NPL; ++j) st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+            }
+        }
+        if (fold) store_rows(static_cast<StT *>(a.state_cache), slot_base, 0u);
+    }
 
     if constexpr (kDepth > 1) {
         // Token inputs (dt, x, B, C) do not depend on the state: they are loaded
@@ -215,6 +327,10 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
 #pragma unroll
                     for (int i = 0; i < kRowsPerWarp; ++i)
                         if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+                }
+                if (live) {
+                    chunk_store(tb + u);
+                    ring_store(tb + u);
                 }
             }
 #pragma unroll
@@ -277,20 +393,17 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                 for (int i = 0; i < kRowsPerWarp; ++i)
                     if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
             }
+            chunk_store(t);
+            ring_store(t);
         }
     }
 
-    if (a.write_final) {
-        StT *out = static_cast<StT *>(a.state_cache);
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i)
-            if (row_ok[i]) store_n<StT, NPL>(out + slot_base + (int64_t)(p0 + i) * a.N + n0, st[i], nvalid, vec);
-    }
+    if (a.write_final) store_rows(static_cast<StT *>(a.state_cache), fslot_base, 0u);
 }
 
-template <typename IoT, typename StT, int NPL, int kDepth>
+template <typename IoT, typename StT, int NPL, int kDepth, bool kFull>
 __global__ void __launch_bounds__(kWarps * 32) recurrent_scan_kernel(ScanArgs a, bool vec) {
-    recurrent_scan<IoT, StT, NPL, kDepth>(a, vec);
+    recurrent_scan<IoT, StT, NPL, kDepth, kFull>(a, vec);
 }
 
 // The plain loop with four state columns per lane (N <= 128) is latency-bound
@@ -299,10 +412,17 @@ __global__ void __launch_bounds__(kWarps * 32) recurrent_scan_kernel(ScanArgs a,
 // registers (MTP: -12 %).
 template <typename IoT, typename StT>
 __global__ void __launch_bounds__(kWarps * 32, 12) recurrent_scan_kernel_n4(ScanArgs a, bool vec) {
-    recurrent_scan<IoT, StT, 4, 1>(a, vec);
+    recurrent_scan<IoT, StT, 4, 1, false>(a, vec);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether a call uses any optional part (then the kFull variant runs).
+bool uses_options(const ScanArgs &a) {
+    return a.final_slot_idx != nullptr || (a.slot_stride != 0 && a.slot_stride != 1) ||
+           a.snap_flag != nullptr || a.out_chunk_states != nullptr || a.sr_seed != nullptr ||
+           a.ring_x != nullptr;
+}
 
 template <typename IoT, typename StT, int NPL>
 cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t stream) {
@@ -310,11 +430,14 @@ cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t st
     // vector accesses need every row start aligned to the vector width
     const bool vec = (a.N % NPL == 0) && (a.P % kRowsPerWarp == 0) && aligned16(a.x) &&
                      aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
-                     aligned16(a.out_intermediate);
-    if constexpr (NPL == 4 && kDepth == 1)
+                     aligned16(a.out_intermediate) && aligned16(a.out_chunk_states) &&
+                     aligned16(a.snap_states) && aligned16(a.ring_x) && aligned16(a.ring_B);
+    if (uses_options(a))
+        recurrent_scan_kernel<IoT, StT, NPL, kDepth, true><<<grid, block, 0, stream>>>(a, vec);
+    else if constexpr (NPL == 4 && kDepth == 1)
         recurrent_scan_kernel_n4<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
     else
-        recurrent_scan_kernel<IoT, StT, NPL, kDepth><<<grid, block, 0, stream>>>(a, vec);
+        recurrent_scan_kernel<IoT, StT, NPL, kDepth, false><<<grid, block, 0, stream>>>(a, vec);
     return cudaGetLastError();
 }
 

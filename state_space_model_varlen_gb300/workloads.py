@@ -194,7 +194,30 @@ WORKLOADS = {
     "continued_a": "1 seq x 32 tokens from a bf16 512-slot cache (N(0,0.1)), H128 P64 N128 G8, in-place writeback",
     "continued_b": "3 seqs [32, 600, 1600] from a bf16 512-slot cache (N(0,0.1)), H128 P64 N128 G8, in-place writeback",
     "mtp": "128 requests x 3 tokens from a 512-slot fp32 cache (N(0,0.1)), H128 P64 N128 G8, per-token states, no writeback",
+    "mtp_replay": "the mtp windows verified ReplaySSM-style: checkpoints in the 512-slot fp32 cache, "
+                  "rings of 11 positions (window 8) holding 0-8 pending accepted tokens per request",
 }
+
+REPLAY_CAPACITY = 11     # ring positions per slot: the logical window plus one window of 3
+REPLAY_WINDOW = 8
+
+
+def replay_ring(p: Problem, seed: int, capacity: int = REPLAY_CAPACITY, window: int = REPLAY_WINDOW):
+    """Seeded ring contents for ``p``'s slots (draws only): raw x, dt, B of
+    ``capacity`` positions per slot with the recipe's distributions, a random
+    start and a pending count uniform in [0, window] per request."""
+    rng = np.random.default_rng(seed)
+    n = p.num_slots * capacity
+    H, P, N, G = p.nheads, p.headdim, p.dstate, p.ngroups
+    x = rng.standard_normal((n, H, P), dtype=np.float32)
+    dt = np.clip(rng.standard_normal((n, H), dtype=np.float32), -DT_CLIP, DT_CLIP)
+    B = rng.standard_normal((n, G, N), dtype=np.float32) / np.float32(math.sqrt(N))
+    return {"x": to_storage(x, p.io_dtype).reshape(p.num_slots, capacity, H, P),
+            "dt": dt.reshape(p.num_slots, capacity, H),
+            "B": to_storage(B, p.io_dtype).reshape(p.num_slots, capacity, G, N),
+            "window": window,
+            "start": rng.integers(0, capacity, size=p.num_seqs).astype(np.int32),
+            "count": rng.integers(0, window + 1, size=p.num_seqs).astype(np.int32)}
 
 
 def workload(name: str, *, seed: Optional[int] = None, seq_subset=None) -> Problem:
@@ -221,10 +244,11 @@ def workload(name: str, *, seed: Optional[int] = None, seq_subset=None) -> Probl
         p = make_problem([32, 600, 1600], nheads=128, headdim=64, dstate=128, ngroups=8,
                          chunk_size=128, state_dtype="bf16", num_slots=512, has_init=True,
                          cache_std=0.1, seed=3 if seed is None else seed, name=name)
-    elif name == "mtp":
+    elif name in ("mtp", "mtp_replay"):
         p = make_problem([3] * 128, nheads=128, headdim=64, dstate=128, ngroups=8, chunk_size=128,
-                         num_slots=512, has_init=True, write_final=False, want_intermediate=True,
-                         cache_std=0.1, seed=4 if seed is None else seed, name=name)
+                         num_slots=512, has_init=True, write_final=False,
+                         want_intermediate=(name == "mtp"), cache_std=0.1,
+                         seed=4 if seed is None else seed, name=name)
     else:
         raise KeyError(name)
     if seq_subset is not None:

@@ -34,12 +34,14 @@ def test_library_exports_every_declared_symbol():
         assert re.search(r"\bT %s$" % name, out, re.M), name
 
 
-def test_params_struct_layout_matches_c(tmp_path):
-    fields = [f[0] for f in binding.ScanParams._fields_]
+@pytest.mark.parametrize("cls,cname", [(binding.ScanParams, "ssd_scan_params"),
+                                       (binding.ReplayParams, "ssd_replay_params")])
+def test_params_struct_layout_matches_c(tmp_path, cls, cname):
+    fields = [f[0] for f in cls._fields_]
     prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "%s"' % HEADER,
-            "int main(void){", 'printf("%zu\\n", sizeof(ssd_scan_params));']
+            "int main(void){", 'printf("%%zu\\n", sizeof(%s));' % cname]
     for f in fields:
-        prog.append('printf("%%zu\\n", offsetof(ssd_scan_params, %s));' % f)
+        prog.append('printf("%%zu\\n", offsetof(%s, %s));' % (cname, f))
     prog.append("return 0;}")
     c = tmp_path / "layout.c"
     c.write_text("\n".join(prog))
@@ -47,9 +49,9 @@ def test_params_struct_layout_matches_c(tmp_path):
     subprocess.run(["gcc", str(c), "-o", str(exe)], check=True)
     vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
                                            check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(binding.ScanParams)
+    assert vals[0] == ctypes.sizeof(cls)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(binding.ScanParams, f).offset == off, f
+        assert getattr(cls, f).offset == off, f
 
 
 def _params(**kw):
@@ -126,3 +128,58 @@ def test_workspace_layout(S, H, expect):
     else:
         assert size == r256(4 * S)
     assert size <= r256(4 * S) * 2 + 256 + 16384 + (64 << 20)
+
+
+def test_snapshot_workspace_and_launch_count():
+    """Several sequences with initial states and final writeback may cross slots:
+    the workspace grows by int32 flags [S] and S states (cache dtype), 256-byte
+    aligned after the tensor-core part, and the call takes the prep launch; a
+    caller promise of disjoint slots drops both."""
+    base = _params(total_tokens=0, num_seqs=3)
+    with_init = _params(total_tokens=0, num_seqs=3, has_init=0x1000)
+    disjoint = _params(total_tokens=0, num_seqs=3, has_init=0x1000, slots_disjoint=1)
+    r256 = lambda v: (v + 255) // 256 * 256
+    state = 4 * 64 * 128 * 4
+    w0 = binding.workspace_size(base)                  # the tensor-core path's own part
+    assert w0 % 256 == 0
+    assert binding.workspace_size(with_init) == w0 + r256(4 * 3) + 3 * state
+    assert binding.workspace_size(disjoint) == w0
+    one = _params(total_tokens=0, num_seqs=1, has_init=0x1000)
+    assert binding.workspace_size(one) == binding.workspace_size(_params(total_tokens=0, num_seqs=1))
+    rec = _params(total_tokens=0, num_seqs=3, has_init=0x1000, io_dtype=binding.SSD_F32)
+    assert binding.kernel_path(rec) == "recurrent"
+    assert binding.workspace_size(rec) == r256(4 * 3) + 3 * state
+    assert binding.num_launches(rec) == 2
+
+
+def test_option_argument_checks():
+    assert binding.load().ssd_scan_varlen(ctypes.byref(_params(slot_idx_stride=-1)), None) == \
+        binding.SSD_ERR_INVALID_ARG
+    assert binding.load().ssd_scan_varlen(ctypes.byref(_params(out_chunk_states=0x2000)), None) == \
+        binding.SSD_ERR_INVALID_ARG                    # no cu_chunks
+    assert binding.load().ssd_scan_varlen(
+        ctypes.byref(_params(final_slot_idx=0x2000, write_final=0)), None) == binding.SSD_ERR_INVALID_ARG
+    # per-chunk states on the tensor-core path need 128-token multiples
+    p = _params(total_tokens=0, out_chunk_states=0x2000, cu_chunks=0x3000, num_chunk_rows=4,
+                chunk_size=64)
+    assert binding.kernel_path(p) == "recurrent"
+    p.chunk_size = 256
+    assert binding.kernel_path(p) == "chunked_tc"
+
+
+def test_replay_argument_checks():
+    lib = binding.load()
+    r = binding.ReplayParams()
+    r.scan = _params(write_final=0)
+    for name in ("ring_x", "ring_dt", "ring_B", "ring_start", "ring_count"):
+        setattr(r, name, 0x4000)
+    r.ring_start_out, r.ring_count_out = 0x5000, 0x6000
+    r.ring_capacity, r.ring_window = 8, 5
+    r.scan.max_seqlen = 4                               # 5 + 4 > 8: the window does not fit
+    assert lib.ssd_replay_mtp(ctypes.byref(r), None) == binding.SSD_ERR_INVALID_ARG
+    r.scan.max_seqlen = 3
+    r.scan.write_final = 1                              # replay never writes final states
+    assert lib.ssd_replay_mtp(ctypes.byref(r), None) == binding.SSD_ERR_INVALID_ARG
+    r.scan.write_final = 0
+    r.ring_start_out = 0x4000                           # aliases ring_start
+    assert lib.ssd_replay_mtp(ctypes.byref(r), None) == binding.SSD_ERR_INVALID_ARG

@@ -220,8 +220,10 @@ def test_tensor_core_path_is_taken_for_bf16_prefill():
     assert outr["path"] == "chunked_tc" and outr["launches"] == 2
     q = W.make_problem([3, 3], nheads=4, headdim=64, dstate=128, ngroups=2, num_slots=4,
                        has_init=True, seed=46)
-    outq = Hn.run_gpu(q, max_seqlen=3)
+    outq = Hn.run_gpu(q, max_seqlen=3, slots_disjoint=True)
     assert outq["path"] == "recurrent" and outq["launches"] == 1
+    # without the caller's promise of disjoint slots the snapshot pass runs first
+    assert Hn.run_gpu(q, max_seqlen=3)["launches"] == 2
 
 
 def test_many_short_sequences_and_empty_ones():

@@ -39,7 +39,7 @@ def _run(p, noalloc):
         d["x"], d["dt"], d["A"], d["B"], d["C"], d["cu_seqlens"], dt_bias=d["dt_bias"], D=d["D"],
         state_cache=d["state_cache"], slot_idx=d["slot_idx"], has_init=d["has_init"],
         write_final=p.write_final, out_y=y, dt_softplus=p.dt_softplus, chunk_size=p.chunk_size,
-        max_seqlen=p.max_seqlen)
+        max_seqlen=p.max_seqlen, slots_disjoint=True)     # distinct slots: no snapshot needed
     assert binding.kernel_path(params) == "chunked_tc"
     lib = binding.load()
     stream = torch.cuda.current_stream().cuda_stream
@@ -71,13 +71,19 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
-    """More sequences than the fixed scratch holds: clear error, nothing enqueued."""
+    """More sequences than the fixed scratch holds on the tensor-core path (the
+    one that uses scratch; zero tokens keep the path choice on the host): clear
+    error, nothing enqueued.  A call that would need the snapshot of initial
+    states is rejected the same way, unless the caller declares disjoint slots."""
     p = binding.ScanParams()
-    p.total_tokens, p.num_seqs = 10, binding.SSD_NOALLOC_MAX_SEQS + 1
+    p.total_tokens, p.num_seqs = 0, binding.SSD_NOALLOC_MAX_SEQS + 1
     p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = 4, 64, 128, 2, 128
     p.io_dtype, p.state_dtype, p.dt_softplus, p.write_final, p.num_slots = 1, 0, 1, 1, 4
     for name in ("x", "dt", "A", "B", "C", "cu_seqlens", "state_cache", "slot_idx", "out_y"):
         setattr(p, name, 0x1000)
+    assert binding.kernel_path(p) == "chunked_tc"
     rc = binding.load().ssd_scan_varlen_noalloc(ctypes.byref(p), None)
     assert rc == binding.SSD_ERR_SCRATCH_LIMIT
     assert "scratch" in binding.status_string(rc)
+    p.num_seqs, p.has_init = 3, 0x1000          # crossed slots possible: needs a snapshot
+    assert binding.load().ssd_scan_varlen_noalloc(ctypes.byref(p), None) == binding.SSD_ERR_SCRATCH_LIMIT
