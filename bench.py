@@ -80,11 +80,16 @@ def replay_bytes(p, ring) -> int:
     return int(b)
 
 
+TC_BLOCK = 128   # tokens per block of the tensor-core kernel, whatever chunk_size is
+
+
 def algorithmic_flops(p) -> int:
-    """Chunked-SSD contraction work with causal halves counted (per chunk and
-    head: 2lNP chunk state + 2lNP C.h_prev + P l(l+1) masked scores.X; per
-    chunk and group: N l(l+1) for C.B^T)."""
-    L, H, P, N, G = p.chunk_size, p.nheads, p.headdim, p.dstate, p.ngroups
+    """Chunked-SSD contraction work with causal halves counted (per block and
+    head: 2lNP block state + 2lNP C.h_prev + P l(l+1) masked scores.X; per
+    block and group: N l(l+1) for C.B^T), for the 128-token blocks the
+    tensor-core kernel runs (chunk_size only sets where checkpoint states are
+    written; the scan's result does not depend on it beyond rounding)."""
+    L, H, P, N, G = TC_BLOCK, p.nheads, p.headdim, p.dstate, p.ngroups
     f = 0
     for l_seq in p.seqlens:
         l_seq = int(l_seq)

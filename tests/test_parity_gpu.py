@@ -104,11 +104,31 @@ def test_d_zero_varlen_batch_with_initial_states():
     _check_d_zero(p)
 
 
-@pytest.mark.parametrize("chunk", [64, 128, 256])
-def test_chunk_size_invariance(chunk):
-    p = W.make_problem([300, 45], nheads=4, headdim=64, dstate=128, ngroups=1, chunk_size=chunk,
-                       num_slots=4, seed=40)
-    _run_and_check(p)
+def test_block_alignment_invariance():
+    """The tensor-core kernel cuts every sequence into 128-token blocks counted
+    from the sequence's own first token.  The same sequences packed after a
+    filler of 0, 1, 64 or 127 tokens (so at every alignment mod 128) must give
+    bit-identical y and final states."""
+    base = W.make_problem([300, 129, 45], nheads=4, headdim=64, dstate=128, ngroups=1,
+                          num_slots=8, has_init=[1, 0, 1], cache_std=0.1, seed=40)
+    outs = []
+    for off in (0, 1, 64, 127):
+        filler = W.make_problem([off], nheads=4, headdim=64, dstate=128, ngroups=1,
+                                num_slots=8, seed=140 + off)
+        p = W.select_sequences(base, [0, 1, 2])
+        # prepend the filler's tokens as a sequence of its own (slot 7, no initial state)
+        cat = lambda a, b: np.concatenate([a, b])
+        p.x, p.dt, p.B, p.C = cat(filler.x, p.x), cat(filler.dt, p.dt), cat(filler.B, p.B), cat(filler.C, p.C)
+        p.cu_seqlens = np.concatenate([[0], off + base.cu_seqlens]).astype(np.int32)
+        p.slot_idx = np.concatenate([[7], base.slot_idx]).astype(np.int32)
+        p.has_init = np.concatenate([[0], base.has_init]).astype(np.uint8)
+        out = Hn.run_gpu(p, slots_disjoint=True)
+        assert out["status"] == 0 and out["path"] == "chunked_tc"
+        outs.append((out["y"][off:], out["cache"][base.slot_idx]))
+    for y, cache in outs[1:]:
+        np.testing.assert_array_equal(y, outs[0][0])
+        np.testing.assert_array_equal(cache, outs[0][1])
+    Hn.check_y(outs[0][0], oracle.ssd_scan_reference(base)["y"], base.io_dtype)
 
 
 def test_sequence_permutation_bit_identical():
