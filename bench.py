@@ -111,6 +111,7 @@ def _peaks():
 # The sources the tensor-core scan kernel is compiled from (its translation unit
 # and the headers it includes): a DRAM-traffic capture stays valid while they do.
 _SCAN_KERNEL_SOURCES = ("state_space_model_varlen_gb300/csrc/sm100.cuh",
+                        "state_space_model_varlen_gb300/csrc/ssd_common.cuh",
                         "state_space_model_varlen_gb300/csrc/ssd_chunked.cu",
                         "state_space_model_varlen_gb300/csrc/ssd_internal.h",
                         "include/ssd_scan.h")
