@@ -108,8 +108,9 @@ __device__ __forceinline__ float softplus_f(float z) {
     return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
 }
 
-// kDepth: tokens of input prefetched ahead of the recurrence (a register ring;
-// deeper for narrow states, where registers are cheap and the chain is short).
+// kDepth: tokens whose y reductions are batched on the staged narrow-state path
+// (kDepth > 1: inputs staged through shared memory a chunk at a time); 1 for
+// wide states (plain loop, occupancy hides the loads).
 // kFull: the optional parts of a call (separate final slots, strided slot
 // indices, snapshot reads, per-chunk states, stochastic rounding, the
 // ReplaySSM ring) are compiled in; calls without them run the plain variant,
@@ -124,7 +125,9 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const int h = (int)((bid / pblocks) % a.H);
     const int s = (int)(bid / ((int64_t)pblocks * a.H));
     const int p0 = pb * kRowsPerCta + warp * kRowsPerWarp;
-    if (p0 >= a.P) return;                                   // warp-uniform
+    // warps without rows of their own leave early, except on the staged
+    // narrow-state path, where every warp loads and meets at the barriers
+    if (kDepth == 1 && p0 >= a.P) return;
     const int g = h / a.heads_per_group;
 
     // ---- sequence metadata, checked on the device (loads issued together) ----
@@ -275,81 +278,132 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     }
 
     if constexpr (kDepth > 1) {
-        // Token inputs (dt, x, B, C) do not depend on the state: they are loaded
-        // kDepth tokens ahead into a register ring, so the sequential chain waits
-        // on arithmetic, not on memory latency.
-        float rd[kDepth], rx[kDepth][kRowsPerWarp], rb[kDepth][NPL], rc[kDepth][NPL];
-        auto fetch = [&](int u, int64_t t) {
-            if (t < t1) {
-                rd[u] = a.dt[t * a.H + h];
-                load_n<IoT, kRowsPerWarp>(X + (t * a.H + h) * a.P + p0, rx[u], a.P - p0, vec);
-                const int64_t brow = (t * a.G + g) * a.N;
-                load_n<IoT, NPL>(Bm + brow + n0, rb[u], nvalid, vec);
-                load_n<IoT, NPL>(Cm + brow + n0, rc[u], nvalid, vec);
+        // Narrow states (N <= 64): a token's state update is a few FMAs, so its
+        // inputs would dominate if each token's loads were waited for one by one.
+        // All four warps load the inputs (dt, x of the CTA's 16 rows, B, C) of
+        // kStage tokens at a time into shared memory together -- the next chunk
+        // is loaded into registers while the current one is computed and stored
+        // behind it -- and each warp runs its rows' recurrence out of shared
+        // memory, kDepth tokens at a time with their y reductions batched.
+        constexpr int kStage = 32;
+        constexpr int kNMax = 32 * NPL;
+        constexpr int kThr = kWarps * 32;
+        constexpr int kXe = kStage * kRowsPerCta / kThr;        // x elements per thread
+        constexpr int kBe = kStage * kNMax / kThr;              // B (and C) elements per thread
+        static_assert(kStage % kDepth == 0 && kStage <= kThr, "chunk layout");
+        __shared__ float s_dt[2][kStage];
+        __shared__ float s_x[2][kStage][kRowsPerCta];
+        __shared__ __align__(16) float s_b[2][kStage][kNMax];
+        __shared__ __align__(16) float s_c[2][kStage][kNMax];
+        const int tid = threadIdx.x;
+        const int pc0 = pb * kRowsPerCta;                       // first row of the CTA
+        float rdt, rx[kXe], rb[kBe], rc[kBe];
+        auto fetch = [&](int64_t tb) {                          // global -> registers
+            const int64_t td = tb + tid;
+            rdt = (tid < kStage && td < t1) ? a.dt[td * a.H + h] : 0.f;
+#pragma unroll
+            for (int k = 0; k < kXe; ++k) {
+                const int e = tid + k * kThr, tt = e / kRowsPerCta, r = e % kRowsPerCta;
+                const int64_t t = tb + tt;
+                rx[k] = (t < t1 && pc0 + r < a.P) ? to_f(X[(t * a.H + h) * a.P + pc0 + r]) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < kBe; ++k) {
+                const int e = tid + k * kThr, tt = e / kNMax, n = e % kNMax;
+                const int64_t t = tb + tt;
+                const bool v = t < t1 && n < a.N;
+                rb[k] = v ? to_f(Bm[(t * a.G + g) * a.N + n]) : 0.f;
+                rc[k] = v ? to_f(Cm[(t * a.G + g) * a.N + n]) : 0.f;
             }
         };
+        auto put = [&](int buf) {                               // registers -> shared memory
+            if (tid < kStage) s_dt[buf][tid] = rdt;
 #pragma unroll
-        for (int u = 0; u < kDepth; ++u) fetch(u, t0 + u);
-
-        for (int64_t tb = t0; tb < t1; tb += kDepth) {
-            // the group's dt activations, decays and inputs, then the refill; only
-            // the state update below is sequential, the rest is independent work
-            float dd[kDepth], dec[kDepth], xs[kDepth][kRowsPerWarp], bs[kDepth][NPL], cs[kDepth][NPL];
-#pragma unroll
-            for (int u = 0; u < kDepth; ++u) {
-                const float z = rd[u] + bias;
-                dd[u] = a.dt_softplus ? softplus_f(z) : z;
-                dec[u] = expf(dd[u] * Ah);
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) xs[u][i] = rx[u][i];
-#pragma unroll
-                for (int j = 0; j < NPL; ++j) { bs[u][j] = rb[u][j]; cs[u][j] = rc[u][j]; }
+            for (int k = 0; k < kXe; ++k) {
+                const int e = tid + k * kThr;
+                s_x[buf][e / kRowsPerCta][e % kRowsPerCta] = rx[k];
             }
 #pragma unroll
-            for (int u = 0; u < kDepth; ++u) fetch(u, tb + kDepth + u);   // tokens of the next group
-            float part[kDepth][kRowsPerWarp];
+            for (int k = 0; k < kBe; ++k) {
+                const int e = tid + k * kThr;
+                s_b[buf][e / kNMax][e % kNMax] = rb[k];
+                s_c[buf][e / kNMax][e % kNMax] = rc[k];
+            }
+        };
+        const int xr0 = warp * kRowsPerWarp;                    // this warp's rows within the CTA's
+        fetch(t0);
+        put(0);
+        __syncthreads();
+        int buf = 0;
+        for (int64_t cb = t0; cb < t1; cb += kStage) {
+            const bool more = cb + kStage < t1;
+            if (more) fetch(cb + kStage);                       // next chunk, in flight meanwhile
+#pragma unroll 1
+            for (int ub = 0; ub < kStage; ub += kDepth) {
+                const int64_t tb = cb + ub;
+                if (tb >= t1) break;
+                float dd[kDepth], dec[kDepth], xs[kDepth][kRowsPerWarp];
 #pragma unroll
-            for (int u = 0; u < kDepth; ++u) {
-                const bool live = tb + u < t1;
+                for (int u = 0; u < kDepth; ++u) {
+                    const float z = s_dt[buf][ub + u] + bias;
+                    dd[u] = a.dt_softplus ? softplus_f(z) : z;
+                    dec[u] = expf(dd[u] * Ah);
 #pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) {
-                    const float dx = dd[u] * xs[u][i];
-                    float acc = 0.f;
+                    for (int i = 0; i < kRowsPerWarp; ++i) xs[u][i] = s_x[buf][ub + u][xr0 + i];
+                }
+                float part[kDepth][kRowsPerWarp];
+#pragma unroll
+                for (int u = 0; u < kDepth; ++u) {
+                    const bool live = tb + u < t1;
+                    float bs[NPL], cs[NPL];
 #pragma unroll
                     for (int j = 0; j < NPL; ++j) {
-                        if (live) st[i][j] = fmaf(dec[u], st[i][j], dx * bs[u][j]);
-                        acc = fmaf(cs[u][j], st[i][j], acc);
+                        bs[j] = s_b[buf][ub + u][n0 + j];
+                        cs[j] = s_c[buf][ub + u][n0 + j];
                     }
-                    part[u][i] = acc;
+#pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i) {
+                        const float dx = dd[u] * xs[u][i];
+                        float acc = 0.f;
+#pragma unroll
+                        for (int j = 0; j < NPL; ++j) {
+                            if (live) st[i][j] = fmaf(dec[u], st[i][j], dx * bs[j]);
+                            acc = fmaf(cs[j], st[i][j], acc);
+                        }
+                        part[u][i] = acc;
+                    }
+                    if (live && inter) {
+                        const int64_t ibase = (((tb + u) * a.H + h) * a.P + p0) * a.N;
+#pragma unroll
+                        for (int i = 0; i < kRowsPerWarp; ++i)
+                            if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+                    }
+                    if (live) {
+                        chunk_store(tb + u);
+                        ring_store(tb + u);
+                    }
                 }
-                if (live && inter) {
-                    const int64_t ibase = (((tb + u) * a.H + h) * a.P + p0) * a.N;
+#pragma unroll
+                for (int u = 0; u < kDepth; ++u)
 #pragma unroll
                     for (int i = 0; i < kRowsPerWarp; ++i)
-                        if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
-                }
-                if (live) {
-                    chunk_store(tb + u);
-                    ring_store(tb + u);
-                }
-            }
 #pragma unroll
-            for (int u = 0; u < kDepth; ++u)
+                        for (int off = 16; off > 0; off >>= 1)
+                            part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i], off);
 #pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i)
+                for (int u = 0; u < kDepth; ++u) {
+                    if (tb + u < t1 && lane < kRowsPerWarp && row_ok[lane]) {
+                        float yv = 0.f;
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i], off);
-#pragma unroll
-            for (int u = 0; u < kDepth; ++u) {
-                if (tb + u < t1 && lane < kRowsPerWarp && row_ok[lane]) {
-                    float yv = 0.f;
-#pragma unroll
-                    for (int i = 0; i < kRowsPerWarp; ++i)
-                        if (i == lane) yv = part[u][i] + Dh * xs[u][i];
-                    Y[((tb + u) * a.H + h) * a.P + p0 + lane] = from_f<IoT>(yv);
+                        for (int i = 0; i < kRowsPerWarp; ++i)
+                            if (i == lane) yv = part[u][i] + Dh * xs[u][i];
+                        Y[((tb + u) * a.H + h) * a.P + p0 + lane] = from_f<IoT>(yv);
+                    }
                 }
             }
+            if (more) put(buf ^ 1);
+            __syncthreads();                                    // every warp is done with buf
+            buf ^= 1;
         }
     } else {
         // wide states: registers are scarce, plain loop (occupancy hides latency)
