@@ -125,9 +125,10 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     const int h = (int)((bid / pblocks) % a.H);
     const int s = (int)(bid / ((int64_t)pblocks * a.H));
     const int p0 = pb * kRowsPerCta + warp * kRowsPerWarp;
-    // warps without rows of their own leave early, except on the staged
-    // narrow-state path, where every warp loads and meets at the barriers
-    if (kDepth == 1 && p0 >= a.P) return;
+    // warps without rows of their own leave early, except where every warp
+    // loads inputs for the CTA and meets at barriers (the staged narrow-state
+    // path, the ReplaySSM prologue)
+    if (kDepth == 1 && p0 >= a.P && !(kFull && a.ring_x != nullptr)) return;
     const int g = h / a.heads_per_group;
 
     // ---- sequence metadata, checked on the device (loads issued together) ----
@@ -257,22 +258,60 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         }
     };
     if (replay) {
-        // advance the checkpoint through the pending ring inputs (no output)
-        for (int32_t j = 0; j < rcount; ++j) {
-            const int64_t rrow = (int64_t)slot * a.ring_capacity + (rstart + j) % a.ring_capacity;
-            const float z = a.ring_dt[rrow * a.H + h] + bias;
-            const float d = a.dt_softplus ? softplus_f(z) : z;
-            const float decay = expf(d * Ah);
-            float xv[kRowsPerWarp], bv[NPL];
-            load_n<IoT, kRowsPerWarp>(static_cast<const IoT *>(a.ring_x) + (rrow * a.H + h) * a.P + p0, xv,
-                                      a.P - p0, vec);
-            load_n<IoT, NPL>(static_cast<const IoT *>(a.ring_B) + (rrow * a.G + g) * a.N + n0, bv, nvalid, vec);
+        // advance the checkpoint through the pending ring inputs (no output):
+        // the CTA loads kRs tokens' inputs at a time into shared memory
+        // together, every load in flight at once, then each warp replays them
+        // for its rows
+        constexpr int kRs = 8;
+        constexpr int kNM = 32 * NPL;
+        constexpr int kThr = kWarps * 32;
+        __shared__ float rs_dt[kRs];
+        __shared__ float rs_x[kRs][kRowsPerCta];
+        __shared__ __align__(16) float rs_b[kRs][kNM];
+        const int tid = threadIdx.x, pc0 = pb * kRowsPerCta, xr0 = warp * kRowsPerWarp;
+        const IoT *RX = static_cast<const IoT *>(a.ring_x);
+        const IoT *RB = static_cast<const IoT *>(a.ring_B);
+        auto rrow = [&](int32_t j) { return (int64_t)slot * a.ring_capacity + (rstart + j) % a.ring_capacity; };
+        for (int32_t j0 = 0; j0 < rcount; j0 += kRs) {
+            const int nj = rcount - j0 < kRs ? rcount - j0 : kRs;
+            float vx[kRs * kRowsPerCta / kThr > 0 ? kRs * kRowsPerCta / kThr : 1];
+            float vb[kRs * kNM / kThr];
+            float vd = 0.f;
+            if (tid < nj) vd = a.ring_dt[rrow(j0 + tid) * a.H + h];
 #pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const float dx = d * xv[i];
-#pragma unroll
-                for (int j = 0; j < NPL; ++j) st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+            for (int k = 0; k < kRs * kRowsPerCta / kThr; ++k) {
+                const int e = tid + k * kThr, jj = e / kRowsPerCta, r = e % kRowsPerCta;
+                vx[k] = (jj < nj && pc0 + r < a.P) ? to_f(RX[(rrow(j0 + jj) * a.H + h) * a.P + pc0 + r]) : 0.f;
             }
+#pragma unroll
+            for (int k = 0; k < kRs * kNM / kThr; ++k) {
+                const int e = tid + k * kThr, jj = e / kNM, n = e % kNM;
+                vb[k] = (jj < nj && n < a.N) ? to_f(RB[(rrow(j0 + jj) * a.G + g) * a.N + n]) : 0.f;
+            }
+            if (tid < kRs) rs_dt[tid] = vd;
+#pragma unroll
+            for (int k = 0; k < kRs * kRowsPerCta / kThr; ++k) {
+                const int e = tid + k * kThr;
+                rs_x[e / kRowsPerCta][e % kRowsPerCta] = vx[k];
+            }
+#pragma unroll
+            for (int k = 0; k < kRs * kNM / kThr; ++k) {
+                const int e = tid + k * kThr;
+                rs_b[e / kNM][e % kNM] = vb[k];
+            }
+            __syncthreads();
+            for (int jj = 0; jj < nj; ++jj) {
+                const float z = rs_dt[jj] + bias;
+                const float d = a.dt_softplus ? softplus_f(z) : z;
+                const float decay = expf(d * Ah);
+#pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i) {
+                    const float dx = d * rs_x[jj][xr0 + i];
+#pragma unroll
+                    for (int j = 0; j < NPL; ++j) st[i][j] = fmaf(decay, st[i][j], dx * rs_b[jj][n0 + j]);
+                }
+            }
+            __syncthreads();
         }
         if (fold) store_rows(static_cast<StT *>(a.state_cache), slot_base, 0u);
     }
@@ -469,6 +508,13 @@ __global__ void __launch_bounds__(kWarps * 32, 12) recurrent_scan_kernel_n4(Scan
     recurrent_scan<IoT, StT, 4, 1, false>(a, vec);
 }
 
+// The same shape with the optional parts (ReplaySSM, final slots, ...): eight
+// resident CTAs per SM, so the replay prologue's memory latency overlaps.
+template <typename IoT, typename StT>
+__global__ void __launch_bounds__(kWarps * 32, 8) recurrent_scan_kernel_n4_full(ScanArgs a, bool vec) {
+    recurrent_scan<IoT, StT, 4, 1, true>(a, vec);
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Whether a call uses any optional part (then the kFull variant runs).
@@ -486,8 +532,12 @@ cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t st
                      aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
                      aligned16(a.out_intermediate) && aligned16(a.out_chunk_states) &&
                      aligned16(a.snap_states) && aligned16(a.ring_x) && aligned16(a.ring_B);
-    if (uses_options(a))
-        recurrent_scan_kernel<IoT, StT, NPL, kDepth, true><<<grid, block, 0, stream>>>(a, vec);
+    if (uses_options(a)) {
+        if constexpr (NPL == 4 && kDepth == 1)
+            recurrent_scan_kernel_n4_full<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
+        else
+            recurrent_scan_kernel<IoT, StT, NPL, kDepth, true><<<grid, block, 0, stream>>>(a, vec);
+    }
     else if constexpr (NPL == 4 && kDepth == 1)
         recurrent_scan_kernel_n4<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
     else
