@@ -249,16 +249,24 @@ __device__ __noinline__ Item find_item(const Params &p, const int32_t *order, in
         const int32_t hp = r - rank * hp_per_seq;
         const int32_t seq = order[rank];
         const int32_t h0 = hp * 2;
+        // every per-sequence entry the item may need, loaded together (one
+        // memory round trip instead of a chain of dependent ones)
         const int64_t a = p.cu_seqlens[seq], e = p.cu_seqlens[seq + 1];
+        const bool init_raw = p.has_init != nullptr && p.has_init[seq] != 0;
+        const int32_t slot_raw = p.slot_idx != nullptr ? p.slot_idx[seq * p.slot_stride] : 0;
+        const int32_t fslot_raw = p.final_slot_idx != nullptr ? p.final_slot_idx[seq * p.final_slot_stride] : 0;
+        const bool snap_raw = p.snap_flag != nullptr && p.snap_flag[seq] != 0;
+        const int64_t c0 = p.out_chunk_states ? p.cu_chunks[seq] : 0;
+        const int64_t c1 = p.out_chunk_states ? p.cu_chunks[seq + 1] : 0;
         if (a < 0 || e < a || e > p.T) {
             if (report && j == 0 && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SEQLENS);
             continue;
         }
-        const bool init = p.has_init != nullptr && p.has_init[seq] != 0;
+        const bool init = init_raw;
         int32_t slot = 0, fslot = 0;
         if (init || p.write_final) {
-            slot = p.slot_idx[seq * p.slot_stride];
-            fslot = (p.write_final && p.final_slot_idx) ? p.final_slot_idx[seq * p.final_slot_stride] : slot;
+            slot = slot_raw;
+            fslot = (p.write_final && p.final_slot_idx) ? fslot_raw : slot;
             if ((init && (slot < 0 || slot >= p.num_slots)) ||
                 (p.write_final && (fslot < 0 || fslot >= p.num_slots))) {
                 if (report && j == 0 && p.device_status) atomicOr(p.device_status, SSD_DEV_BAD_SLOT);
@@ -268,13 +276,12 @@ __device__ __noinline__ Item find_item(const Params &p, const int32_t *order, in
         const int32_t len = (int32_t)(e - a);
         int32_t crow = -1;
         if (p.out_chunk_states) {
-            const int64_t c0 = p.cu_chunks[seq], c1 = p.cu_chunks[seq + 1];
             if (c0 >= 0 && c1 - c0 == (len + p.chunk_size - 1) / p.chunk_size && c1 <= p.num_chunk_rows)
                 crow = (int32_t)c0;
             else if (report && j == 0 && p.device_status)
                 atomicOr(p.device_status, SSD_DEV_BAD_CHUNKS);
         }
-        const bool snap = init && p.snap_flag != nullptr && p.snap_flag[seq] != 0;
+        const bool snap = init && snap_raw;
         const int32_t nb = (len + kQ - 1) / kQ;
         const int32_t nseg = nb == 0 ? 1 : (nb + seg - 1) / seg;
         const int32_t b0 = j * seg, b1 = min(nb, (j + 1) * seg);
@@ -1076,6 +1083,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
         bool have = wk.next(sm, c, false, true, status);
         if (have) prefetch_init(c);
         DtRaw dr = have ? dt_load(p, c.row0, c.l, c.h0) : DtRaw{};
+        // the CTA's first block is prepared at once: the lookup of what follows
+        // it may still be in flight on the item warp
+        if (have) {
+            ds = dt_prep(sm, p, dr, c.l, c.h0, c.first, k, ds.R0, ds.R1, status);
+            ++k;
+            have = ds.ok && wk.next(sm, c, false, true, status);
+            if (have) prefetch_init(c);
+            dr = have ? dt_load(p, c.row0, c.l, c.h0) : DtRaw{};
+        }
         while (ds.ok && have) {
             const bool have_n = wk.next(sm, cn, false, true, status);
             if (have_n) prefetch_init(cn);
@@ -1391,9 +1407,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
             }
             const uint32_t ab = kc % kArrBufs;
             const Arrays &ar = sm.arr[ab];
-            if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status))) break;
             if (!c.first) {
-                if (!(ok = warp_wait(sm, &sm.state_done, (kc - 1) & 1, status))) break;
+                if (!(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status) &&
+                           warp_wait(sm, &sm.state_done, (kc - 1) & 1, status)))
+                    break;
                 tc_fence_after();
             } else if (!c.init) {
 #pragma unroll 1
@@ -1436,6 +1453,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_cons
                 }
                 tmem_wait_st();
             }
+            // an item's first block: its initial state is loaded before its scales
+            // are awaited (they come from the dt warp's first pass over the item)
+            if (c.first && !(ok = warp_wait(sm, &sm.arr_ready[ab], (kc / kArrBufs) & 1, status))) break;
             uint32_t packed[64];                  // bf16 copy (hi part) of this lane's 128 state values
             // per head: the state entering the block is hs * eprev; renormalised
             // accumulators hold exp(dlt) h instead.  h = hi + lo with both parts
