@@ -539,29 +539,49 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def _oracle_sample(p, target_s):
-    """Time the fp64 oracle on a bounded sample of ``p``: the first sequences,
-    all heads, sized from a short calibration run to ~target_s seconds."""
-    import numpy as np
+def _oracle_calibrate(p):
+    """Seconds per token and head of the fp64 oracle on this host, from a head
+    slice of the first non-empty sequence of ``p``."""
     import oracle
     from state_space_model_varlen_gb300 import workloads as W
     threads = oracle.max_threads()
-    order = list(range(p.num_seqs))
-    # calibration: a head slice of the first non-empty sequence
-    first = next(s for s in order if p.seqlens[s] > 0)
-    q = W.select_sequences(p, [first])
+    first = next(s for s in range(p.num_seqs) if p.seqlens[s] > 0)
+    q = W.select_sequences(p, [first], compact=True)
     h1 = max(1, min(p.nheads, threads))
     t = time.perf_counter()
     oracle.ssd_scan_reference(q, heads=(0, h1))
-    per_tok_head = (time.perf_counter() - t) / (int(p.seqlens[first]) * h1)
-    budget_tok = target_s / max(per_tok_head, 1e-12) / p.nheads
+    return (time.perf_counter() - t) / (int(p.seqlens[first]) * h1)
+
+
+def _oracle_sample(p, target_s, per_tok_head=None):
+    """Time the fp64 oracle on a bounded sample of ``p`` sized to ~target_s
+    seconds: the first sequences, or, where even one sequence would take
+    longer, a prefix of the first; all heads.  Returns (tokens, seconds,
+    threads, sequences, passes, heads)."""
+    import oracle
+    from state_space_model_varlen_gb300 import workloads as W
+    threads = oracle.max_threads()
+    if per_tok_head is None:
+        per_tok_head = _oracle_calibrate(p)
+    budget = target_s / max(per_tok_head, 1e-12)          # token-heads
+    first = next(s for s in range(p.num_seqs) if p.seqlens[s] > 0)
+    if budget < int(p.seqlens[first]) * p.nheads:
+        # all heads of as long a prefix of the first sequence as the budget
+        # holds (the oracle converts every head's inputs whatever slice it
+        # scans, so a head slice would count less work than it does)
+        ntok = int(min(int(p.seqlens[first]), max(16, budget // p.nheads)))
+        q = W.sequence_prefix(p, first, ntok)
+        t = time.perf_counter()
+        oracle.ssd_scan_reference(q)
+        el = time.perf_counter() - t
+        return q.total_tokens, el, threads, 1, 1, p.nheads
     chosen, tok = [], 0
-    for s in order:
-        if tok >= budget_tok and chosen:
+    for s in range(p.num_seqs):
+        if tok * p.nheads >= budget and chosen:
             break
         chosen.append(s)
         tok += int(p.seqlens[s])
-    q = W.select_sequences(p, chosen)
+    q = W.select_sequences(p, chosen, compact=True)
     # the whole workload may take well under target_s: repeat it until the
     # sample spans most of the budget, so the rate is not a single short run
     passes, el = 0, 0.0
@@ -570,11 +590,11 @@ def _oracle_sample(p, target_s):
         oracle.ssd_scan_reference(q)
         el += time.perf_counter() - t
         passes += 1
-    return q.total_tokens * passes, el, threads, len(chosen), passes
+    return q.total_tokens * passes, el, threads, len(chosen), passes, p.nheads
 
 
 def cpu_baseline(p, target_s):
-    tok, el, threads, nseq, passes = _oracle_sample(p, target_s)
+    tok, el, threads, nseq, passes, _ = _oracle_sample(p, target_s)
     return {"value": tok / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": "%d of %d sequences (all %d heads) of workload %s, %d pass(es), %d tokens, fp64, %.1f s"
                       % (nseq, p.num_seqs, p.nheads, p.name, passes, tok, el)}
@@ -585,12 +605,16 @@ def run_reference(args, rank):
     if rank != 0:
         return None
     p = W.workload(args.workload)
-    per_step = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 2)
+    # the whole run (warm-up and timed steps) takes about four times
+    # --cpu-seconds of host time, or 0.1 s a step where that is longer (so that
+    # the oracle's per-call overhead stays a small part of each step)
+    rate = _oracle_calibrate(p)
+    per_step = max(0.1, 4.0 * args.cpu_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        _oracle_sample(p, per_step / 4)
-    tok_total, el_total, threads, nseq = 0, 0.0, 0, 0
+        _oracle_sample(p, per_step, rate)
+    tok_total, el_total, threads, nseq, heads = 0.0, 0.0, 0, 0, 0
     for _ in range(args.steps):
-        tok, el, threads, nseq, _ = _oracle_sample(p, per_step)
+        tok, el, threads, nseq, _, heads = _oracle_sample(p, per_step, rate)
         tok_total += tok
         el_total += el
     value = tok_total / el_total
@@ -604,8 +628,8 @@ def run_reference(args, rank):
                    "chunk_size": p.chunk_size, "io_dtype": p.io_dtype,
                    "state_dtype": p.state_dtype},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": "%d of %d sequences per step, all heads, fp64"
-                                   % (nseq, p.num_seqs)},
+                         "sample": "%d of %d sequences (or a prefix of the first) per step, "
+                                   "all %d heads, fp64" % (nseq, p.num_seqs, heads)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -256,17 +256,38 @@ def workload(name: str, *, seed: Optional[int] = None, seq_subset=None) -> Probl
     return p
 
 
-def select_sequences(p: Problem, seqs) -> Problem:
-    """A new problem made of the listed sequences of ``p`` (same values, repacked)."""
+def sequence_prefix(p: Problem, s: int, ntok: int) -> Problem:
+    """A one-sequence problem: the first ``ntok`` tokens of sequence ``s`` of
+    ``p`` (a prefix is itself a valid sequence), with its cache slots only."""
+    q = select_sequences(p, [s], compact=True)
+    n = max(0, min(int(ntok), q.total_tokens))
+    return dataclasses.replace(q, cu_seqlens=np.array([0, n], dtype=np.int32),
+                               x=q.x[:n], dt=q.dt[:n], B=q.B[:n], C=q.C[:n])
+
+
+def select_sequences(p: Problem, seqs, compact: bool = False) -> Problem:
+    """A new problem made of the listed sequences of ``p`` (same values, repacked).
+    compact: keep only the cache slots those sequences name (in slot order,
+    indices renumbered), instead of a copy of the whole cache."""
     seqs = list(seqs)
     cu = p.cu_seqlens.astype(np.int64)
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs]) if seqs else np.zeros(0, np.int64)
     lens = [int(cu[s + 1] - cu[s]) for s in seqs]
     ncu = np.zeros(len(seqs) + 1, dtype=np.int64)
     ncu[1:] = np.cumsum(lens)
+    slot_idx = p.slot_idx[seqs].copy()
+    final_slot_idx = None if p.final_slot_idx is None else p.final_slot_idx[seqs].copy()
+    if compact:
+        named = slot_idx if final_slot_idx is None else np.concatenate([slot_idx, final_slot_idx])
+        used = np.unique(named.astype(np.int64))
+        cache = p.cache[used]
+        slot_idx = np.searchsorted(used, slot_idx).astype(np.int32)
+        if final_slot_idx is not None:
+            final_slot_idx = np.searchsorted(used, final_slot_idx).astype(np.int32)
+    else:
+        cache = p.cache.copy()
     return dataclasses.replace(
         p, cu_seqlens=ncu.astype(np.int32), x=p.x[rows], dt=p.dt[rows], B=p.B[rows], C=p.C[rows],
-        slot_idx=p.slot_idx[seqs].copy(),
-        final_slot_idx=None if p.final_slot_idx is None else p.final_slot_idx[seqs].copy(),
+        slot_idx=slot_idx, final_slot_idx=final_slot_idx,
         has_init=None if p.has_init is None else p.has_init[seqs].copy(),
-        cache=p.cache.copy())
+        cache=cache)
