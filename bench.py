@@ -400,8 +400,10 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     p = W.workload(args.workload)
     T = p.total_tokens
-    r = _Resident(ssd, p, dev)
+    replay = args.workload == "mtp_replay"
+    r = _ResidentReplay(ssd, p, dev) if replay else _Resident(ssd, p, dev)
     launches, path = r.launches, r.path
+    replay_b = replay_bytes(p, r.ring) if replay else None
     total_ms, clocks, wall, how = _time_device(ssd, r, stream, args.steps, args.warmup, flush,
                                                local_rank, world)
 
@@ -411,12 +413,13 @@ def run_ours(args, rank, world, local_rank):
     pin = lambda t: t.cpu().pin_memory()
     hx, hB, hC, hdt = pin(x), pin(B), pin(C), pin(dt)
     hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    if p.write_final:
+    write_final = p.write_final and not replay
+    if write_final:
         hfinal = torch.empty((p.num_seqs,) + tuple(cache.shape[1:]), dtype=cache.dtype,
                              pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hB, hC, hdt))
     d2h = hy.numel() * hy.element_size() + (hfinal.numel() * hfinal.element_size()
-                                            if p.write_final else 0)
+                                            if write_final else 0)
     if inter is not None:
         hinter = torch.empty(inter.shape, dtype=inter.dtype, pin_memory=True)
         d2h += hinter.numel() * hinter.element_size()
@@ -429,9 +432,9 @@ def run_ours(args, rank, world, local_rank):
         B.copy_(hB, non_blocking=True)
         C.copy_(hC, non_blocking=True)
         dt.copy_(hdt, non_blocking=True)
-        ssd.call(params, sptr)
+        _call(ssd, r, sptr)
         hy.copy_(y, non_blocking=True)
-        if p.write_final:
+        if write_final:
             hfinal.copy_(cache.index_select(0, slots64), non_blocking=True)
         if inter is not None:
             hinter.copy_(inter, non_blocking=True)
@@ -477,10 +480,10 @@ def run_ours(args, rank, world, local_rank):
     tokens_all = T * world
     value = whole_job_rate(T, world, ms_per_step)
     _, tc_peak, _ = _peaks()
-    bytes_per_call = algorithmic_bytes(p)
-    roof = _roofline_entry(p, ms_per_step)
+    bytes_per_call = replay_b if replay else algorithmic_bytes(p)
+    roof = _roofline_entry(p, ms_per_step, bytes_per_call)
     roof.update({
-        "traffic": _traffic_per_launch(args.workload),
+        "traffic": None if replay else _traffic_per_launch(args.workload),
         "algorithmic_flops_per_launch": algorithmic_flops(p),
         "tensor_time_at_peak_us": algorithmic_flops(p) / (tc_peak * 1e12) * 1e6,
         "hbm_time_at_peak_us": bytes_per_call / (roof["peak"] * 1e9) * 1e6,

@@ -244,7 +244,8 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
     // ReplaySSM: the window token t goes to ring position wpos0 + (t - t0)
     auto ring_store = [&](int64_t t) {
         if (!replay) return;
-        const int64_t pos = (wpos0 + (t - t0)) % a.ring_capacity;
+        int64_t pos = wpos0 + (t - t0);             // < 2 capacity: wpos0 < capacity, K <= capacity
+        if (pos >= a.ring_capacity) pos -= a.ring_capacity;
         const int64_t rrow = (int64_t)slot * a.ring_capacity + pos;
         if (lane < kRowsPerWarp && row_ok[lane])
             static_cast<IoT *>(a.ring_x)[(rrow * a.H + h) * a.P + p0 + lane] = X[(t * a.H + h) * a.P + p0 + lane];
@@ -265,13 +266,17 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         constexpr int kRs = 8;
         constexpr int kNM = 32 * NPL;
         constexpr int kThr = kWarps * 32;
-        __shared__ float rs_dt[kRs];
+        __shared__ float rs_d[kRs], rs_dec[kRs];   // dt' and exp(dt' A) of each staged token
         __shared__ float rs_x[kRs][kRowsPerCta];
         __shared__ __align__(16) float rs_b[kRs][kNM];
         const int tid = threadIdx.x, pc0 = pb * kRowsPerCta, xr0 = warp * kRowsPerWarp;
         const IoT *RX = static_cast<const IoT *>(a.ring_x);
         const IoT *RB = static_cast<const IoT *>(a.ring_B);
-        auto rrow = [&](int32_t j) { return (int64_t)slot * a.ring_capacity + (rstart + j) % a.ring_capacity; };
+        auto rrow = [&](int32_t j) {                // j < window <= capacity, rstart < capacity
+            int32_t q = rstart + j;
+            if (q >= a.ring_capacity) q -= a.ring_capacity;
+            return (int64_t)slot * a.ring_capacity + q;
+        };
         for (int32_t j0 = 0; j0 < rcount; j0 += kRs) {
             const int nj = rcount - j0 < kRs ? rcount - j0 : kRs;
             float vx[kRs * kRowsPerCta / kThr > 0 ? kRs * kRowsPerCta / kThr : 1];
@@ -288,7 +293,12 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                 const int e = tid + k * kThr, jj = e / kNM, n = e % kNM;
                 vb[k] = (jj < nj && n < a.N) ? to_f(RB[(rrow(j0 + jj) * a.G + g) * a.N + n]) : 0.f;
             }
-            if (tid < kRs) rs_dt[tid] = vd;
+            if (tid < kRs) {                            // once per CTA, not per warp
+                const float z = vd + bias;
+                const float d = a.dt_softplus ? softplus_f(z) : z;
+                rs_d[tid] = d;
+                rs_dec[tid] = expf(d * Ah);
+            }
 #pragma unroll
             for (int k = 0; k < kRs * kRowsPerCta / kThr; ++k) {
                 const int e = tid + k * kThr;
@@ -301,9 +311,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
             }
             __syncthreads();
             for (int jj = 0; jj < nj; ++jj) {
-                const float z = rs_dt[jj] + bias;
-                const float d = a.dt_softplus ? softplus_f(z) : z;
-                const float decay = expf(d * Ah);
+                const float d = rs_d[jj], decay = rs_dec[jj];
 #pragma unroll
                 for (int i = 0; i < kRowsPerWarp; ++i) {
                     const float dx = d * rs_x[jj][xr0 + i];
