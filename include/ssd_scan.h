@@ -185,12 +185,19 @@ typedef struct {
  * parameters as well; ssd_scan_varlen reports those. */
 size_t ssd_scan_varlen_workspace_size(const ssd_scan_params *params);
 
-/* Enqueue the scan on `stream` (NULL = legacy default stream).  Returns
- * SSD_OK when the kernels were enqueued; launch errors come back as
- * SSD_ERR_CUDA.  Never synchronises. */
+/* Enqueue the scan on `stream` (NULL = legacy default stream): the SSD
+ * recurrence above over every packed sequence of cu_seqlens (vLLM PR #61501
+ * "Details": one varlen scan of the packed batch), initial states read from
+ * their cache slots with snapshot semantics (vLLM PR #62922 "Details") and
+ * final, per-token or per-chunk states written in the cache dtype (vLLM PR
+ * #61501 "Details").  Returns SSD_OK when the kernels were enqueued; invalid
+ * arguments come back as SSD_ERR_* with nothing enqueued, launch errors as
+ * SSD_ERR_CUDA, and faults in device-resident inputs (slots, lengths, chunk
+ * rows) as bits of *device_status.  Never synchronises. */
 ssd_status ssd_scan_varlen(const ssd_scan_params *params, struct CUstream_st *stream);
 
-/* Number of kernels a call with these parameters launches: 0 for an empty
+/* Number of kernels a call with these parameters launches (the pages' path
+ * takes five Triton launches, vLLM PR #61501 "Details"): 0 for an empty
  * batch, else 1 or 2 (the tensor-core path sorts a batch of at most 32
  * sequences that it does not cut into segments inside its one kernel; the
  * choice depends on params->workspace_bytes and the current device's SM
@@ -199,7 +206,8 @@ int32_t ssd_scan_varlen_num_launches(const ssd_scan_params *params);
 
 /* Name of the kernel path a call would take: "chunked_tc" (tcgen05 chunked
  * scan), "recurrent" (token-by-token SIMT scan: fp32 I/O, intermediate
- * states, continuations of at most 3 tokens, other shapes) or "invalid". */
+ * states, continuations of at most 3 tokens -- the MTP verification shape of
+ * vLLM PR #52928 "Summary" -- other shapes) or "invalid". */
 const char *ssd_scan_varlen_path(const ssd_scan_params *params);
 
 /* Maximum number of sequences ssd_scan_varlen_noalloc accepts on the
