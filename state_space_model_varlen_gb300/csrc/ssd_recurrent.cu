@@ -108,6 +108,41 @@ __device__ __forceinline__ float softplus_f(float z) {
     return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
 }
 
+// Sums over the warp's 32 lanes of RPW per-lane partial values, one per p-row,
+// by recursive halving: at each step a lane keeps half of its values plus its
+// partner's copies of that half, so RPW values take RPW - 1 + 5 - log2(RPW)
+// shuffles instead of 5 RPW.  Lane l ends with the sum of row
+// rowsum_row<RPW>(l); the lanes that share a row hold the same sum.
+template <int RPW>
+__device__ __forceinline__ float warp_rowsums(float (&v)[RPW], int lane) {
+    static_assert(RPW >= 1 && RPW <= 32 && (RPW & (RPW - 1)) == 0, "power of two rows");
+#pragma unroll
+    for (int half = RPW / 2, off = 16; half >= 1; half /= 2, off /= 2) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int off = 32 / RPW / 2; off > 0; off /= 2) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+template <int RPW>
+__device__ __forceinline__ int rowsum_row(int lane) {
+    int r = 0;
+#pragma unroll
+    for (int half = RPW / 2, off = 16; half >= 1; half /= 2, off /= 2)
+        if (lane & off) r += half;
+    return r;
+}
+// the first lane of each group that warp_rowsums leaves holding one row's sum
+template <int RPW>
+__device__ __forceinline__ bool rowsum_writer(int lane) { return (lane & (32 / RPW - 1)) == 0; }
+
 // kDepth: tokens whose y reductions are batched on the staged narrow-state path
 // (kDepth > 1: inputs staged through shared memory a chunk at a time); 1 for
 // wide states (plain loop, occupancy hides the loads).
@@ -115,8 +150,10 @@ __device__ __forceinline__ float softplus_f(float z) {
 // indices, snapshot reads, per-chunk states, stochastic rounding, the
 // ReplaySSM ring) are compiled in; calls without them run the plain variant,
 // whose register budget they would otherwise take.
-template <typename IoT, typename StT, int NPL, int kDepth, bool kFull>
+template <typename IoT, typename StT, int NPL, int kDepth, bool kFull, int RPW = 4>
 __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
+    constexpr int kRowsPerWarp = RPW;                   // p-rows of a warp
+    constexpr int kRowsPerCta = kWarps * RPW;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int pblocks = (a.P + kRowsPerCta - 1) / kRowsPerCta;
@@ -247,7 +284,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         int64_t pos = wpos0 + (t - t0);             // < 2 capacity: wpos0 < capacity, K <= capacity
         if (pos >= a.ring_capacity) pos -= a.ring_capacity;
         const int64_t rrow = (int64_t)slot * a.ring_capacity + pos;
-        if (lane < kRowsPerWarp && row_ok[lane])
+        if (lane < kRowsPerWarp && p0 + lane < a.P)
             static_cast<IoT *>(a.ring_x)[(rrow * a.H + h) * a.P + p0 + lane] = X[(t * a.H + h) * a.P + p0 + lane];
         if (pb == 0 && warp == 0) {
             if (lane == 0) a.ring_dt[rrow * a.H + h] = a.dt[t * a.H + h];
@@ -439,7 +476,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                             part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i], off);
 #pragma unroll
                 for (int u = 0; u < kDepth; ++u) {
-                    if (tb + u < t1 && lane < kRowsPerWarp && row_ok[lane]) {
+                    if (tb + u < t1 && lane < kRowsPerWarp && p0 + lane < a.P) {
                         float yv = 0.f;
 #pragma unroll
                         for (int i = 0; i < kRowsPerWarp; ++i)
@@ -468,7 +505,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
 #pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i) {
                 const float dx = d * xv[i];
-                float acc = 0.f;
+                float acc = lane == 0 ? Dh * xv[i] : 0.f;      // D x enters the row sum once
 #pragma unroll
                 for (int j = 0; j < NPL; ++j) {
                     st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
@@ -476,17 +513,10 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                 }
                 part[i] = acc;
             }
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i)
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-            if (lane < kRowsPerWarp && row_ok[lane]) {
-                float yv = 0.f;
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i)
-                    if (i == lane) yv = part[i] + Dh * xv[i];
-                Y[xrow + lane] = from_f<IoT>(yv);
+            {
+                const float yv = warp_rowsums<kRowsPerWarp>(part, lane);
+                const int r = rowsum_row<kRowsPerWarp>(lane);
+                if (rowsum_writer<kRowsPerWarp>(lane) && p0 + r < a.P) Y[xrow + r] = from_f<IoT>(yv);
             }
             if (inter) {
                 const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
@@ -516,6 +546,14 @@ __global__ void __launch_bounds__(kWarps * 32, 12) recurrent_scan_kernel_n4(Scan
     recurrent_scan<IoT, StT, 4, 1, false>(a, vec);
 }
 
+// ReplaySSM verification: sixteen p-rows a warp (all 64 rows of a head in one
+// CTA), so that the ring staging, each token's dt' and decay, and the
+// metadata are shared by four times as many rows.
+template <typename IoT, typename StT>
+__global__ void __launch_bounds__(kWarps * 32, 4) recurrent_replay_kernel_n4(ScanArgs a, bool vec) {
+    recurrent_scan<IoT, StT, 4, 1, true, 16>(a, vec);
+}
+
 // The same shape with the optional parts (ReplaySSM, final slots, ...): eight
 // resident CTAs per SM, so the replay prologue's memory latency overlaps.
 template <typename IoT, typename StT>
@@ -532,14 +570,18 @@ bool uses_options(const ScanArgs &a) {
            a.ring_x != nullptr;
 }
 
+// vector accesses need every row start aligned to the vector width
+bool vec_ok(const ScanArgs &a, int npl, int rows_per_warp) {
+    return (a.N % npl == 0) && (a.P % rows_per_warp == 0) && aligned16(a.x) && aligned16(a.B) &&
+           aligned16(a.C) && aligned16(a.state_cache) && aligned16(a.out_intermediate) &&
+           aligned16(a.out_chunk_states) && aligned16(a.snap_states) && aligned16(a.ring_x) &&
+           aligned16(a.ring_B);
+}
+
 template <typename IoT, typename StT, int NPL>
 cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t stream) {
     constexpr int kDepth = NPL <= 2 ? 4 : 1;
-    // vector accesses need every row start aligned to the vector width
-    const bool vec = (a.N % NPL == 0) && (a.P % kRowsPerWarp == 0) && aligned16(a.x) &&
-                     aligned16(a.B) && aligned16(a.C) && aligned16(a.state_cache) &&
-                     aligned16(a.out_intermediate) && aligned16(a.out_chunk_states) &&
-                     aligned16(a.snap_states) && aligned16(a.ring_x) && aligned16(a.ring_B);
+    const bool vec = vec_ok(a, NPL, kRowsPerWarp);
     if (uses_options(a)) {
         if constexpr (NPL == 4 && kDepth == 1)
             recurrent_scan_kernel_n4_full<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
@@ -560,6 +602,14 @@ cudaError_t launch_npl(const ScanArgs &a, cudaStream_t stream) {
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks), block(kWarps * 32);
+    if (a.ring_x != nullptr && a.N > 64 && a.N <= 128) {
+        // ReplaySSM verification: one CTA per (sequence, head, 64 p-rows)
+        constexpr int kRows = kWarps * 16;
+        const int64_t rblocks = (int64_t)a.S * a.H * ((a.P + kRows - 1) / kRows);
+        if (rblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        recurrent_replay_kernel_n4<IoT, StT><<<(unsigned)rblocks, block, 0, stream>>>(a, vec_ok(a, 4, 16));
+        return cudaGetLastError();
+    }
     if (a.N <= 32) return launch_one<IoT, StT, 1>(a, grid, block, stream);
     if (a.N <= 64) return launch_one<IoT, StT, 2>(a, grid, block, stream);
     if (a.N <= 128) return launch_one<IoT, StT, 4>(a, grid, block, stream);

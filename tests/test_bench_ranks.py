@@ -31,7 +31,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo_world2():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()     # no fork: other tests may have started threads
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
     assert out[0] == [15.0, 3.0] and out[1] == [15.0, 3.0]
