@@ -7,10 +7,12 @@
 // kernel does not cover (fp32 activations, intermediate states, other
 // head/state sizes).
 //
-// Work split: one CTA per (sequence, head, block of 16 p-rows); warp w owns
-// p-rows [4w, 4w+4) of the block and each lane owns NPL consecutive state
-// columns n, so the whole state slice lives in registers (4 x NPL floats per
-// thread) and one token costs one warp-level reduction per p-row for y.
+// Work split: one CTA of four warps per (sequence, head, block of 4 R p-rows);
+// warp w owns p-rows [Rw, Rw+R) of the block (R = 4; 8 for the plain N <= 128
+// kernel, 16 for ReplaySSM) and each lane owns NPL consecutive state columns
+// n, so the whole state slice lives in registers (R x NPL floats per thread).
+// A token's y takes one warp-level sum per p-row; on the wide-state loop the
+// R sums share their shuffles by recursive halving.
 // Warps never synchronise with each other.  The initial state is read
 // straight from the cache slot (no gather, vLLM PR #62922 "Details"), or from
 // the snapshot the snapshot pass took when another sequence of the call writes
@@ -537,13 +539,14 @@ __global__ void __launch_bounds__(kWarps * 32) recurrent_scan_kernel(ScanArgs a,
     recurrent_scan<IoT, StT, NPL, kDepth, kFull>(a, vec);
 }
 
-// The plain loop with four state columns per lane (N <= 128) is latency-bound
-// on its few tokens per CTA: twelve resident CTAs per SM (40 registers, a few
-// spills to L1) keep more loads and stores in flight than seven CTAs of 72
-// registers (MTP: -12 %).
+// The plain loop with four state columns per lane (N <= 128) streams its
+// states (MTP: the state after every token): eight p-rows a warp and eight
+// resident CTAs per SM (64 registers, a few spills to L1) keep more state
+// stores in flight per warp than four rows at twelve CTAs (MTP: -9 %), and
+// share each token's dt', decay and B, C loads over twice the rows.
 template <typename IoT, typename StT>
-__global__ void __launch_bounds__(kWarps * 32, 12) recurrent_scan_kernel_n4(ScanArgs a, bool vec) {
-    recurrent_scan<IoT, StT, 4, 1, false>(a, vec);
+__global__ void __launch_bounds__(kWarps * 32, 8) recurrent_scan_kernel_n4(ScanArgs a, bool vec) {
+    recurrent_scan<IoT, StT, 4, 1, false, 8>(a, vec);
 }
 
 // ReplaySSM verification: sixteen p-rows a warp (all 64 rows of a head in one
@@ -588,9 +591,12 @@ cudaError_t launch_one(const ScanArgs &a, dim3 grid, dim3 block, cudaStream_t st
         else
             recurrent_scan_kernel<IoT, StT, NPL, kDepth, true><<<grid, block, 0, stream>>>(a, vec);
     }
-    else if constexpr (NPL == 4 && kDepth == 1)
-        recurrent_scan_kernel_n4<IoT, StT><<<grid, block, 0, stream>>>(a, vec);
-    else
+    else if constexpr (NPL == 4 && kDepth == 1) {
+        constexpr int kRows = kWarps * 8;                   // p-rows of a CTA of this kernel
+        const int64_t nb = (int64_t)a.S * a.H * ((a.P + kRows - 1) / kRows);
+        if (nb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        recurrent_scan_kernel_n4<IoT, StT><<<(unsigned)nb, block, 0, stream>>>(a, vec_ok(a, 4, 8));
+    } else
         recurrent_scan_kernel<IoT, StT, NPL, kDepth, false><<<grid, block, 0, stream>>>(a, vec);
     return cudaGetLastError();
 }
