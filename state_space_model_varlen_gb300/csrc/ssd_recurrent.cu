@@ -493,16 +493,9 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         }
     } else {
         // wide states: registers are scarce, plain loop (occupancy hides latency)
-        for (int64_t t = t0; t < t1; ++t) {
-            const float z = a.dt[t * a.H + h] + bias;
-            const float d = a.dt_softplus ? softplus_f(z) : z;
-            const float decay = expf(d * Ah);
-            float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+        auto step = [&](int64_t t, float d, float decay, const float (&xv)[kRowsPerWarp],
+                        const float (&bv)[NPL], const float (&cv)[NPL]) {
             const int64_t xrow = (t * a.H + h) * a.P + p0;
-            load_n<IoT, kRowsPerWarp>(X + xrow, xv, a.P - p0, vec);
-            const int64_t brow = (t * a.G + g) * a.N;
-            load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
-            load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
             float part[kRowsPerWarp];
 #pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -528,6 +521,86 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
             }
             chunk_store(t);
             ring_store(t);
+        };
+        bool staged = false;
+        if constexpr (kFull) {
+            if (replay) {
+                // ReplaySSM window: its tokens' inputs staged through shared
+                // memory kWs tokens at a time, every load in flight together
+                // (the window's first chunk alongside nothing else to wait for)
+                staged = true;
+                constexpr int kWs = 8;
+                constexpr int kNM = 32 * NPL;
+                constexpr int kThr = kWarps * 32;
+                constexpr int kXe = kWs * kRowsPerCta / kThr > 0 ? kWs * kRowsPerCta / kThr : 1;
+                __shared__ float ws_d[kWs], ws_dec[kWs];
+                __shared__ float ws_x[kWs][kRowsPerCta];
+                __shared__ __align__(16) float ws_b[kWs][kNM];
+                __shared__ __align__(16) float ws_c[kWs][kNM];
+                const int tid = threadIdx.x, pc0 = pb * kRowsPerCta, xr0 = warp * kRowsPerWarp;
+                for (int64_t tb = t0; tb < t1; tb += kWs) {
+                    const int nj = t1 - tb < kWs ? (int)(t1 - tb) : kWs;
+                    float vx[kXe], vb[kWs * kNM / kThr], vc[kWs * kNM / kThr];
+                    float vd = 0.f;
+                    if (tid < nj) vd = a.dt[(tb + tid) * a.H + h];
+#pragma unroll
+                    for (int k = 0; k < kXe; ++k) {
+                        const int e = tid + k * kThr, jj = e / kRowsPerCta, r = e % kRowsPerCta;
+                        vx[k] = (jj < nj && pc0 + r < a.P) ? to_f(X[((tb + jj) * a.H + h) * a.P + pc0 + r]) : 0.f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kWs * kNM / kThr; ++k) {
+                        const int e = tid + k * kThr, jj = e / kNM, n = e % kNM;
+                        const bool v = jj < nj && n < a.N;
+                        const int64_t row = ((tb + jj) * a.G + g) * a.N + n;
+                        vb[k] = v ? to_f(Bm[row]) : 0.f;
+                        vc[k] = v ? to_f(Cm[row]) : 0.f;
+                    }
+                    if (tid < kWs) {                            // once per CTA, not per warp
+                        const float z = vd + bias;
+                        const float d = a.dt_softplus ? softplus_f(z) : z;
+                        ws_d[tid] = d;
+                        ws_dec[tid] = expf(d * Ah);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kXe; ++k) {
+                        const int e = tid + k * kThr;
+                        if (e < kWs * kRowsPerCta) ws_x[e / kRowsPerCta][e % kRowsPerCta] = vx[k];
+                    }
+#pragma unroll
+                    for (int k = 0; k < kWs * kNM / kThr; ++k) {
+                        const int e = tid + k * kThr;
+                        ws_b[e / kNM][e % kNM] = vb[k];
+                        ws_c[e / kNM][e % kNM] = vc[k];
+                    }
+                    __syncthreads();
+                    for (int jj = 0; jj < nj; ++jj) {
+                        float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+#pragma unroll
+                        for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = ws_x[jj][xr0 + i];
+#pragma unroll
+                        for (int j = 0; j < NPL; ++j) {
+                            bv[j] = ws_b[jj][n0 + j];
+                            cv[j] = ws_c[jj][n0 + j];
+                        }
+                        step(tb + jj, ws_d[jj], ws_dec[jj], xv, bv, cv);
+                    }
+                    __syncthreads();
+                }
+            }
+        }
+        if (!staged) {
+            for (int64_t t = t0; t < t1; ++t) {
+                const float z = a.dt[t * a.H + h] + bias;
+                const float d = a.dt_softplus ? softplus_f(z) : z;
+                const float decay = expf(d * Ah);
+                float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+                load_n<IoT, kRowsPerWarp>(X + (t * a.H + h) * a.P + p0, xv, a.P - p0, vec);
+                const int64_t brow = (t * a.G + g) * a.N;
+                load_n<IoT, NPL>(Bm + brow + n0, bv, nvalid, vec);
+                load_n<IoT, NPL>(Cm + brow + n0, cv, nvalid, vec);
+                step(t, d, decay, xv, bv, cv);
+            }
         }
     }
 
