@@ -297,7 +297,132 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                             Bm[(t * a.G + g) * a.N + n0 + j];
         }
     };
-    if (replay) {
+    // one token of the recurrence for this warp's rows, with y and the
+    // optional per-token, per-chunk and ring writes
+    auto step = [&](int64_t t, float d, float decay, const float (&xv)[kRowsPerWarp],
+                    const float (&bv)[NPL], const float (&cv)[NPL]) {
+        const int64_t xrow = (t * a.H + h) * a.P + p0;
+        float part[kRowsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const float dx = d * xv[i];
+            float acc = lane == 0 ? Dh * xv[i] : 0.f;      // D x enters the row sum once
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+                st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
+                acc = fmaf(cv[j], st[i][j], acc);
+            }
+            part[i] = acc;
+        }
+        {
+            const float yv = warp_rowsums<kRowsPerWarp>(part, lane);
+            const int r = rowsum_row<kRowsPerWarp>(lane);
+            if (rowsum_writer<kRowsPerWarp>(lane) && p0 + r < a.P) Y[xrow + r] = from_f<IoT>(yv);
+        }
+        if (inter) {
+            const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i)
+                if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
+        }
+        chunk_store(t);
+        ring_store(t);
+    };
+    // ReplaySSM on a full head (N = 128, the CTA owning all P rows): the
+    // pending ring tokens and the window tokens are staged through shared
+    // memory together with asynchronous copies (one memory round trip for up
+    // to kTs tokens, no register staging), then replayed in order: the ring
+    // part advances the checkpoint (folded into the cache when the window
+    // overflows the ring), the window part produces y.
+    bool unified = false;
+    if constexpr (kFull && kDepth == 1 && NPL == 4 && RPW == 16) {
+        if (replay && a.N == 32 * NPL && a.P == kRowsPerCta && vec) {
+            unified = true;
+            constexpr int kTs = 16;
+            constexpr int kNM = 32 * NPL;
+            constexpr int kThr = kWarps * 32;
+            constexpr int kCx = kRowsPerCta * (int)sizeof(IoT) / 16;   // 16-byte chunks of a token's x
+            constexpr int kCb = kNM * (int)sizeof(IoT) / 16;           // ... of its B (and C) row
+            __shared__ __align__(16) IoT u_x[kTs][kRowsPerCta];
+            __shared__ __align__(16) IoT u_b[kTs][kNM];
+            __shared__ __align__(16) IoT u_c[kTs][kNM];
+            __shared__ __align__(16) float u_dt[kTs];
+            __shared__ float u_d[kTs], u_dec[kTs];
+            const int tid = threadIdx.x, xr0 = warp * kRowsPerWarp;
+            const IoT *RX = static_cast<const IoT *>(a.ring_x);
+            const IoT *RB = static_cast<const IoT *>(a.ring_B);
+            const int32_t ntot = rcount + (int32_t)(t1 - t0);
+            auto rrow = [&](int32_t j) {                // j < window <= capacity, rstart < capacity
+                int32_t q = rstart + j;
+                if (q >= a.ring_capacity) q -= a.ring_capacity;
+                return (int64_t)slot * a.ring_capacity + q;
+            };
+            auto cp16 = [](void *dst, const void *src) {
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                             "l"(src) : "memory");
+            };
+            if (fold && rcount == 0) store_rows(static_cast<StT *>(a.state_cache), slot_base, 0u);
+            for (int32_t j0 = 0; j0 < ntot; j0 += kTs) {
+                const int nj = ntot - j0 < kTs ? ntot - j0 : kTs;
+                for (int e = tid; e < nj * (kCx + 2 * kCb); e += kThr) {
+                    const int jj = e / (kCx + 2 * kCb), c = e % (kCx + 2 * kCb), j = j0 + jj;
+                    const bool ring = j < rcount;
+                    if (c < kCx) {
+                        const IoT *src = ring ? RX + (rrow(j) * a.H + h) * a.P
+                                              : X + ((t0 + j - rcount) * a.H + h) * a.P;
+                        cp16(&u_x[jj][c * 16 / (int)sizeof(IoT)], src + c * 16 / (int)sizeof(IoT));
+                    } else if (c < kCx + kCb) {
+                        const int cb = c - kCx;
+                        const IoT *src = ring ? RB + (rrow(j) * a.G + g) * a.N
+                                              : Bm + ((t0 + j - rcount) * a.G + g) * a.N;
+                        cp16(&u_b[jj][cb * 16 / (int)sizeof(IoT)], src + cb * 16 / (int)sizeof(IoT));
+                    } else if (!ring) {
+                        const int cc = c - kCx - kCb;
+                        cp16(&u_c[jj][cc * 16 / (int)sizeof(IoT)],
+                             Cm + ((t0 + j - rcount) * a.G + g) * a.N + cc * 16 / (int)sizeof(IoT));
+                    }
+                }
+                if (tid < nj) {
+                    const int j = j0 + tid;
+                    u_dt[tid] = j < rcount ? a.ring_dt[rrow(j) * a.H + h] : a.dt[(t0 + j - rcount) * a.H + h];
+                }
+                asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+                __syncthreads();
+                if (tid < nj) {                             // once per CTA, not per warp
+                    const float z = u_dt[tid] + bias;
+                    const float d = a.dt_softplus ? softplus_f(z) : z;
+                    u_d[tid] = d;
+                    u_dec[tid] = expf(d * Ah);
+                }
+                __syncthreads();
+                for (int jj = 0; jj < nj; ++jj) {
+                    const int j = j0 + jj;
+                    const float d = u_d[jj], decay = u_dec[jj];
+                    if (j < rcount) {
+#pragma unroll
+                        for (int i = 0; i < kRowsPerWarp; ++i) {
+                            const float dx = d * to_f(u_x[jj][xr0 + i]);
+#pragma unroll
+                            for (int q = 0; q < NPL; ++q) st[i][q] = fmaf(decay, st[i][q], dx * to_f(u_b[jj][n0 + q]));
+                        }
+                        if (j == rcount - 1 && fold) store_rows(static_cast<StT *>(a.state_cache), slot_base, 0u);
+                    } else {
+                        float xv[kRowsPerWarp], bv[NPL], cv[NPL];
+#pragma unroll
+                        for (int i = 0; i < kRowsPerWarp; ++i) xv[i] = to_f(u_x[jj][xr0 + i]);
+#pragma unroll
+                        for (int q = 0; q < NPL; ++q) {
+                            bv[q] = to_f(u_b[jj][n0 + q]);
+                            cv[q] = to_f(u_c[jj][n0 + q]);
+                        }
+                        step(t0 + j - rcount, d, decay, xv, bv, cv);
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    }
+    if (replay && !unified) {
         // advance the checkpoint through the pending ring inputs (no output):
         // the CTA loads kRs tokens' inputs at a time into shared memory
         // together, every load in flight at once, then each warp replays them
@@ -493,38 +618,9 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         }
     } else {
         // wide states: registers are scarce, plain loop (occupancy hides latency)
-        auto step = [&](int64_t t, float d, float decay, const float (&xv)[kRowsPerWarp],
-                        const float (&bv)[NPL], const float (&cv)[NPL]) {
-            const int64_t xrow = (t * a.H + h) * a.P + p0;
-            float part[kRowsPerWarp];
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const float dx = d * xv[i];
-                float acc = lane == 0 ? Dh * xv[i] : 0.f;      // D x enters the row sum once
-#pragma unroll
-                for (int j = 0; j < NPL; ++j) {
-                    st[i][j] = fmaf(decay, st[i][j], dx * bv[j]);
-                    acc = fmaf(cv[j], st[i][j], acc);
-                }
-                part[i] = acc;
-            }
-            {
-                const float yv = warp_rowsums<kRowsPerWarp>(part, lane);
-                const int r = rowsum_row<kRowsPerWarp>(lane);
-                if (rowsum_writer<kRowsPerWarp>(lane) && p0 + r < a.P) Y[xrow + r] = from_f<IoT>(yv);
-            }
-            if (inter) {
-                const int64_t ibase = ((t * a.H + h) * a.P + p0) * a.N;
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i)
-                    if (row_ok[i]) store_n<StT, NPL>(inter + ibase + (int64_t)i * a.N + n0, st[i], nvalid, vec);
-            }
-            chunk_store(t);
-            ring_store(t);
-        };
-        bool staged = false;
+        bool staged = unified;
         if constexpr (kFull) {
-            if (replay) {
+            if (replay && !unified) {
                 // ReplaySSM window: its tokens' inputs staged through shared
                 // memory kWs tokens at a time, every load in flight together
                 // (the window's first chunk alongside nothing else to wait for)
