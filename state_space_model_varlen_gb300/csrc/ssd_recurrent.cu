@@ -328,15 +328,15 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
         chunk_store(t);
         ring_store(t);
     };
-    // ReplaySSM on a full head (N = 128, the CTA owning all P rows): the
-    // pending ring tokens and the window tokens are staged through shared
-    // memory together with asynchronous copies (one memory round trip for up
-    // to kTs tokens, no register staging), then replayed in order: the ring
-    // part advances the checkpoint (folded into the cache when the window
-    // overflows the ring), the window part produces y.
+    // Wide states (N = 128) with eight or sixteen rows a warp: the tokens'
+    // inputs are staged through shared memory with asynchronous copies, up to
+    // kTs tokens in one memory round trip with no register staging, then run
+    // in order.  For ReplaySSM the pending ring tokens come first and advance
+    // the checkpoint (folded into the cache when the window overflows the
+    // ring), then the window tokens produce y; for MTP it is the window alone.
     bool unified = false;
-    if constexpr (kFull && kDepth == 1 && NPL == 4 && RPW == 16) {
-        if (replay && a.N == 32 * NPL && a.P == kRowsPerCta && vec) {
+    if constexpr (kDepth == 1 && NPL == 4 && RPW >= 8) {
+        if (a.N == 32 * NPL && a.P % kRowsPerCta == 0 && vec) {
             unified = true;
             constexpr int kTs = 16;
             constexpr int kNM = 32 * NPL;
@@ -348,7 +348,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
             __shared__ __align__(16) IoT u_c[kTs][kNM];
             __shared__ __align__(16) float u_dt[kTs];
             __shared__ float u_d[kTs], u_dec[kTs];
-            const int tid = threadIdx.x, xr0 = warp * kRowsPerWarp;
+            const int tid = threadIdx.x, xr0 = warp * kRowsPerWarp, pc0 = pb * kRowsPerCta;
             const IoT *RX = static_cast<const IoT *>(a.ring_x);
             const IoT *RB = static_cast<const IoT *>(a.ring_B);
             const int32_t ntot = rcount + (int32_t)(t1 - t0);
@@ -368,8 +368,8 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                     const int jj = e / (kCx + 2 * kCb), c = e % (kCx + 2 * kCb), j = j0 + jj;
                     const bool ring = j < rcount;
                     if (c < kCx) {
-                        const IoT *src = ring ? RX + (rrow(j) * a.H + h) * a.P
-                                              : X + ((t0 + j - rcount) * a.H + h) * a.P;
+                        const IoT *src = (ring ? RX + (rrow(j) * a.H + h) * a.P
+                                               : X + ((t0 + j - rcount) * a.H + h) * a.P) + pc0;
                         cp16(&u_x[jj][c * 16 / (int)sizeof(IoT)], src + c * 16 / (int)sizeof(IoT));
                     } else if (c < kCx + kCb) {
                         const int cb = c - kCx;
