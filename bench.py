@@ -276,7 +276,10 @@ class _Resident:
             self.x, self.dt, A, self.B, self.C, cu, dt_bias=bias, D=D, state_cache=self.cache,
             slot_idx=self.slots, has_init=has_init, write_final=p.write_final, out_y=self.y,
             out_intermediate=self.inter, dt_softplus=p.dt_softplus, chunk_size=p.chunk_size,
-            max_seqlen=p.max_seqlen, device_status=self.status)
+            max_seqlen=p.max_seqlen, device_status=self.status,
+            # each sequence owns its slot (the serving case): the caller says so,
+            # which spares the snapshot of initial states
+            slots_disjoint=p.final_slot_idx is None and len(set(p.slot_idx.tolist())) == p.num_seqs)
         need = ssd.workspace_size(self.params)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         self.params.workspace, self.params.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
