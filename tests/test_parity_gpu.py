@@ -144,6 +144,23 @@ def test_sequence_permutation_bit_identical():
         np.testing.assert_array_equal(outq["cache"][p.slot_idx[s]], out["cache"][p.slot_idx[s]])
 
 
+@pytest.mark.parametrize("P,N,io,lens", [
+    (64, 128, "bf16", [3, 3, 2, 40]),       # eight rows a warp, staged asynchronously, > 16 tokens
+    (64, 128, "f32", [3, 1, 3]),            # the same with fp32 inputs
+    (48, 96, "bf16", [3, 2, 3]),            # rows not a multiple of the CTA's: register-free plain loop
+    (64, 100, "bf16", [2, 3]),              # N not 128: the plain loop
+])
+def test_token_path_variants_with_per_token_states(P, N, io, lens):
+    """The token-by-token kernel's wide-state variants, with the state after
+    every token written (the MTP shape) and initial states from the cache."""
+    p = W.make_problem(lens, nheads=4, headdim=P, dstate=N, ngroups=2, io_dtype=io,
+                       num_slots=len(lens) + 2, has_init=True, want_intermediate=True,
+                       cache_std=0.1, seed=50 + P + N + len(lens))
+    out = Hn.run_gpu(p, max_seqlen=3 if max(lens) <= 3 else 0)
+    assert out["path"] == "recurrent"
+    Hn.check_all(p, out, oracle.ssd_scan_reference(p))
+
+
 def test_short_path_hint_agrees_with_general_path():
     p = W.make_problem([3, 2, 1, 3], nheads=8, headdim=64, dstate=128, ngroups=2, num_slots=8,
                        has_init=True, cache_std=0.1, seed=42)

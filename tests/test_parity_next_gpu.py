@@ -192,15 +192,16 @@ def test_stochastic_rounding_is_unbiased_over_seeds():
 # --------------------------------------------------------------------------
 # ReplaySSM verification step
 # --------------------------------------------------------------------------
-def _replay_case(S, K, seed, H=8, G=2, R=11, window=8, state_dtype="f32", counts=None, io="bf16"):
-    p = W.make_problem([K] * S, nheads=H, headdim=64, dstate=128, ngroups=G, io_dtype=io,
+def _replay_case(S, K, seed, H=8, G=2, R=11, window=8, state_dtype="f32", counts=None, io="bf16",
+                 P=64, N=128):
+    p = W.make_problem([K] * S, nheads=H, headdim=P, dstate=N, ngroups=G, io_dtype=io,
                        state_dtype=state_dtype, num_slots=S + 3, has_init=True, write_final=False,
                        cache_std=0.1, seed=seed)
     rng = np.random.default_rng(seed + 1)
     T = R * p.num_slots
-    q = W.make_problem([T], nheads=H, headdim=64, dstate=128, ngroups=G, io_dtype=io, rng=rng)
-    ring = {"x": q.x.reshape(p.num_slots, R, H, 64), "dt": q.dt.reshape(p.num_slots, R, H),
-            "B": q.B.reshape(p.num_slots, R, G, 128), "window": window,
+    q = W.make_problem([T], nheads=H, headdim=P, dstate=N, ngroups=G, io_dtype=io, rng=rng)
+    ring = {"x": q.x.reshape(p.num_slots, R, H, P), "dt": q.dt.reshape(p.num_slots, R, H),
+            "B": q.B.reshape(p.num_slots, R, G, N), "window": window,
             "start": rng.integers(0, R, size=S),
             "count": np.asarray(counts if counts is not None else rng.integers(0, window + 1, size=S))}
     return p, ring
@@ -232,6 +233,21 @@ def _check_replay(p, ring):
 
 def test_replay_step_matches_oracle():
     p, ring = _replay_case(12, 3, seed=84, counts=[0, 1, 2, 3, 4, 5, 6, 7, 8, 0, 5, 6])
+    _check_replay(p, ring)
+
+
+@pytest.mark.parametrize("P,N,io,K,R", [
+    (64, 128, "f32", 3, 11),       # fp32 inputs through the asynchronous staging
+    (32, 128, "bf16", 3, 11),      # a CTA wider than the head: staged through registers
+    (64, 64, "bf16", 3, 11),       # narrow states: the generic kernel's replay prologue
+    (64, 128, "bf16", 12, 22),     # a window longer than one 16-token staging round
+])
+def test_replay_other_shapes_match_oracle(P, N, io, K, R):
+    """Every kernel variant the replay step can take: the full-head kernel
+    with asynchronous staging (bf16 and fp32 inputs, windows longer than one
+    staging round), its register-staged fallback, and the generic kernel."""
+    p, ring = _replay_case(6, K, seed=90 + P + N + K, P=P, N=N, io=io, R=R, window=8,
+                           counts=[0, 1, 8, 5, 8, 3])
     _check_replay(p, ring)
 
 
