@@ -562,7 +562,7 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
 #pragma unroll
                     for (int i = 0; i < kRowsPerWarp; ++i) xs[u][i] = s_x[buf][ub + u][xr0 + i];
                 }
-                float part[kDepth][kRowsPerWarp];
+                float part[kDepth * kRowsPerWarp];            // [token u][row i] at u R + i
 #pragma unroll
                 for (int u = 0; u < kDepth; ++u) {
                     const bool live = tb + u < t1;
@@ -575,13 +575,13 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
 #pragma unroll
                     for (int i = 0; i < kRowsPerWarp; ++i) {
                         const float dx = dd[u] * xs[u][i];
-                        float acc = 0.f;
+                        float acc = lane == 0 ? Dh * xs[u][i] : 0.f;   // D x enters the row sum once
 #pragma unroll
                         for (int j = 0; j < NPL; ++j) {
                             if (live) st[i][j] = fmaf(dec[u], st[i][j], dx * bs[j]);
                             acc = fmaf(cs[j], st[i][j], acc);
                         }
-                        part[u][i] = acc;
+                        part[u * kRowsPerWarp + i] = acc;
                     }
                     if (live && inter) {
                         const int64_t ibase = (((tb + u) * a.H + h) * a.P + p0) * a.N;
@@ -594,22 +594,13 @@ __device__ __forceinline__ void recurrent_scan(const ScanArgs &a, bool vec) {
                         ring_store(tb + u);
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < kDepth; ++u)
-#pragma unroll
-                    for (int i = 0; i < kRowsPerWarp; ++i)
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i], off);
-#pragma unroll
-                for (int u = 0; u < kDepth; ++u) {
-                    if (tb + u < t1 && lane < kRowsPerWarp && p0 + lane < a.P) {
-                        float yv = 0.f;
-#pragma unroll
-                        for (int i = 0; i < kRowsPerWarp; ++i)
-                            if (i == lane) yv = part[u][i] + Dh * xs[u][i];
-                        Y[((tb + u) * a.H + h) * a.P + p0 + lane] = from_f<IoT>(yv);
-                    }
+                {
+                    // the kDepth x R row sums share their shuffles (recursive halving)
+                    constexpr int kSums = kDepth * kRowsPerWarp;
+                    const float yv = warp_rowsums<kSums>(part, lane);
+                    const int r = rowsum_row<kSums>(lane), u = r / kRowsPerWarp, i = r % kRowsPerWarp;
+                    if (rowsum_writer<kSums>(lane) && tb + u < t1 && p0 + i < a.P)
+                        Y[((tb + u) * a.H + h) * a.P + p0 + i] = from_f<IoT>(yv);
                 }
             }
             if (more) put(buf ^ 1);
